@@ -1,0 +1,135 @@
+"""ctypes wrapper of the CPU oracle (liboracle.so, built from tide_oracle.c).
+
+TEST INFRASTRUCTURE.  Only tests/, the smoke check and the benchmark's
+CPU-baseline / reference leg may import this package.  The product library
+and its Python binding never import it and never fall back to it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liboracle.so")
+MAX_RANKS = 4096
+_lib = None
+
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        L.oracle_chunk_rows.restype = ctypes.c_int64
+        L.oracle_chunk_rows.argtypes = [ctypes.c_int64, ctypes.c_int32]
+        L.oracle_valid_rows.restype = ctypes.c_int64
+        L.oracle_valid_rows.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+        L.oracle_layout.restype = ctypes.c_int
+        L.oracle_layout.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, _i64p]
+        L.oracle_rs_element.restype = ctypes.c_float
+        L.oracle_rs_element.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_float]
+        L.oracle_rs.restype = None
+        L.oracle_rs.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float]
+        L.oracle_ag_place.restype = None
+        L.oracle_ag_place.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                      ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_ag_source_index.restype = ctypes.c_int64
+        L.oracle_ag_source_index.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_int64]
+        _lib = L
+    return _lib
+
+
+def _dims(shapes):
+    d0, inner = [], []
+    for s in shapes:
+        if len(s) == 0:
+            d0.append(1)
+            inner.append(1)
+            continue
+        n = 1
+        for d in s[1:]:
+            n *= int(d)
+        d0.append(int(s[0]))
+        inner.append(n)
+    return np.asarray(d0, dtype=np.int64), np.asarray(inner, dtype=np.int64)
+
+
+def _ptrs(arrays):
+    return np.asarray([a.ctypes.data for a in arrays], dtype=np.uint64)
+
+
+def chunk_rows(d0: int, n: int) -> int:
+    return lib().oracle_chunk_rows(d0, n)
+
+
+def valid_rows(d0: int, n: int, r: int) -> int:
+    return lib().oracle_valid_rows(d0, n, r)
+
+
+def layout(shapes, num_ranks: int, align: int = 8):
+    """(offsets[P], S) of the rank-major block layout."""
+    d0, inner = _dims(shapes)
+    offs = np.zeros(max(len(shapes), 1), dtype=np.int64)
+    S = ctypes.c_int64(0)
+    rc = lib().oracle_layout(len(shapes), d0.ctypes.data, inner.ctypes.data, num_ranks, align,
+                             offs.ctypes.data, ctypes.byref(S))
+    if rc:
+        raise ValueError("oracle_layout rejected its arguments")
+    return offs[: len(shapes)].copy(), S.value
+
+
+def shard_numel(shape, num_ranks: int) -> int:
+    d0, inner = _dims([shape])
+    return chunk_rows(int(d0[0]), num_ranks) * int(inner[0])
+
+
+def rs_element(vals_bf16: np.ndarray, scale: float) -> float:
+    v = np.ascontiguousarray(vals_bf16, dtype=np.uint16)
+    return lib().oracle_rs_element(v.size, v.ctypes.data, scale)
+
+
+def rs(shapes, num_ranks: int, grads, scale: float):
+    """grads[k][p]: uint16 arrays (bf16 bits).  Returns shards[r][p] fp32 arrays."""
+    if num_ranks > MAX_RANKS:
+        raise ValueError("oracle supports at most 4096 ranks")
+    P = len(shapes)
+    d0, inner = _dims(shapes)
+    g = [np.ascontiguousarray(grads[k][p], dtype=np.uint16)
+         for k in range(num_ranks) for p in range(P)]
+    shards = [[np.empty(chunk_rows(int(d0[p]), num_ranks) * int(inner[p]), dtype=np.float32)
+               for p in range(P)] for _ in range(num_ranks)]
+    flat_out = [shards[r][p] for r in range(num_ranks) for p in range(P)]
+    gp, op = _ptrs(g), _ptrs(flat_out)
+    lib().oracle_rs(num_ranks, P, d0.ctypes.data, inner.ctypes.data, gp.ctypes.data,
+                    op.ctypes.data, scale)
+    return shards
+
+
+def ag_place(shapes, num_ranks: int, gathered: np.ndarray, offsets, block_numel: int):
+    """Returns params[p] (uint16 bf16 bits) placed from the rank-major buffer."""
+    P = len(shapes)
+    d0, inner = _dims(shapes)
+    buf = np.ascontiguousarray(gathered, dtype=np.uint16)
+    assert buf.size >= num_ranks * block_numel
+    offs = np.ascontiguousarray(offsets, dtype=np.int64)
+    params = [np.empty(int(d0[p]) * int(inner[p]), dtype=np.uint16) for p in range(P)]
+    pp = _ptrs(params)
+    lib().oracle_ag_place(num_ranks, P, d0.ctypes.data, inner.ctypes.data, offs.ctypes.data,
+                          block_numel, buf.ctypes.data, pp.ctypes.data)
+    return params
+
+
+def ag_source_index(num_ranks, shape, offset, block_numel, i, j) -> int:
+    d0, inner = _dims([shape])
+    return lib().oracle_ag_source_index(num_ranks, int(d0[0]), int(inner[0]), offset,
+                                        block_numel, i, j)

@@ -1,0 +1,9 @@
+"""The CPU oracle against its pins (no GPU)."""
+import pytest
+
+import oracle_pins
+
+
+@pytest.mark.parametrize("check", oracle_pins.ALL_CHECKS, ids=lambda f: f.__name__)
+def test_oracle_pin(check):
+    check()

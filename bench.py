@@ -1,0 +1,573 @@
+"""Benchmark of the layout-aware reduce-scatter + placement hot path.
+
+One step = one reduce-scatter (N simulated ranks' per-parameter bf16
+gradients -> every rank's fp32 dim-0 shards) plus one all-gather placement
+(rank-major bf16 buffer -> per-parameter storage) over one synthetic
+workload, through the C ABI.  Default workload: the Llama-3.1-70B-shaped
+decoder layer, N = 8.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                  [--impl tide|reference]
+
+Prints ONE JSON line on rank 0.  Under torchrun (--gpus > 1) every rank runs
+an independent replica on its own GPU (the path has no cross-GPU step on one
+box); value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "RS / AG-placement HBM GB/s and % of GB300 peak; concurrent GEMM slowdown %"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
+KERNEL_SRC = os.path.join(ROOT, "layout_aware_collectives_gb300", "csrc", "kernels.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="llama70b")
+    ap.add_argument("--impl", default="tide", choices=["tide", "reference"])
+    ap.add_argument("--no-interference", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(n):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def stop(self, t0=None, t1=None):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sel = [ln for ts, ln in self.lines if t0 is None or (t0 - 0.06 <= ts <= t1 + 0.06)]
+        if not sel:
+            sel = [ln for _, ln in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in sel:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """Per-launch DRAM bytes of the reduce-scatter kernel from the committed
+    ncu summary, or None when absent or taken on another kernel source."""
+    try:
+        src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+        with open(PROFILE_TRAFFIC) as f:
+            for ln in f:
+                parts = ln.split()
+                if len(parts) == 4 and parts[0] == workload and parts[1] == "rs":
+                    if parts[2] == src_hash:
+                        return int(parts[3])
+    except OSError:
+        pass
+    return None
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def oracle_sample(wl, budget_s, max_elems=48 * 2**20):
+    """A bounded sample of the workload for the CPU oracle: every parameter
+    with its rows capped at R (at least N, so every rank owns rows), R chosen
+    so one oracle pass takes about budget_s seconds and the sample holds at
+    most max_elems elements per rank."""
+    import synth
+
+    n = wl.num_ranks
+
+    def shapes_for(R):
+        return [s if not s else (min(int(s[0]), R),) + tuple(int(d) for d in s[1:])
+                for s in wl.shapes]
+
+    def elems(shapes):
+        return sum(synth.numel(s) for s in shapes)
+
+    cal = shapes_for(n)
+    rate = max(1, elems(cal)) / max(time_oracle_pass(wl, cal), 1e-6)
+    R = n
+    while True:
+        nxt = shapes_for(R * 2)
+        if nxt == shapes_for(R) or elems(nxt) / rate > budget_s or elems(nxt) > max_elems:
+            break
+        R *= 2
+    return shapes_for(R)
+
+
+def _sample_inputs(wl, shapes):
+    import numpy as np
+
+    import synth
+    import oracle
+
+    sub = synth.Workload(wl.name + "_sample", wl.num_ranks, shapes, wl.names, wl.sigma, wl.seed,
+                         wl.outlier_every, wl.outlier_mult, wl.zero_groups, wl.zero_pct)
+    grads = [[sub.host_grad_at(k, p, np.arange(synth.numel(s))) for p, s in enumerate(shapes)]
+             for k in range(wl.num_ranks)]
+    offs, S = oracle.layout(shapes, wl.num_ranks, 8)
+    buf = np.full(wl.num_ranks * S, synth.SENTINEL_BF16, dtype=np.uint16)
+    for p, s in enumerate(shapes):
+        d0, inner = synth.dim0_inner(s)
+        c = -(-d0 // wl.num_ranks)
+        full = sub.host_param_value(p)
+        for r in range(wl.num_ranks):
+            v = max(0, min(c, d0 - r * c)) * inner
+            buf[r * S + offs[p]: r * S + offs[p] + v] = full[r * c * inner: r * c * inner + v]
+    return grads, buf, offs, S
+
+
+def time_oracle_pass(wl, shapes, inputs=None):
+    import oracle
+
+    grads, buf, offs, S = inputs if inputs is not None else _sample_inputs(wl, shapes)
+    t0 = time.perf_counter()
+    oracle.rs(shapes, wl.num_ranks, grads, wl.scale)
+    oracle.ag_place(shapes, wl.num_ranks, buf, offs, S)
+    return time.perf_counter() - t0
+
+
+def sample_bytes(wl, shapes):
+    import synth
+
+    psi = sum(synth.numel(s) for s in shapes)
+    return 2 * wl.num_ranks * psi + 4 * psi + 4 * psi
+
+
+def describe_sample(wl, shapes):
+    import synth
+
+    cap = max((s[0] for s in shapes if s), default=1)
+    return (f"{wl.name} (N={wl.num_ranks}): all {len(shapes)} parameters with dim 0 capped at "
+            f"{cap} rows, {sum(synth.numel(s) for s in shapes)} elements per rank; one "
+            "reduce-scatter + one placement pass of the single-threaded C oracle")
+
+
+def cpu_baseline(wl, budget_s):
+    """The oracle, as it stands, on a bounded sample: passes repeated until
+    about budget_s seconds of single-thread CPU work."""
+    shapes = oracle_sample(wl, budget_s)
+    inputs = _sample_inputs(wl, shapes)
+    total, passes = 0.0, 0
+    while total < budget_s or passes == 0:
+        total += time_oracle_pass(wl, shapes, inputs)
+        passes += 1
+    return {"value": round(sample_bytes(wl, shapes) * passes / total / 1e9, 4), "unit": "GB/s",
+            "cores": 1, "kind": "oracle",
+            "sample": describe_sample(wl, shapes) + f"; {passes} passes",
+            "seconds": round(total, 2), "host_cores": cpu_cores()}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import synth
+
+    wl = synth.WORKLOADS[args.config]()
+    per_step = max(0.05, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    shapes = oracle_sample(wl, per_step)
+    inputs = _sample_inputs(wl, shapes)
+    for _ in range(args.warmup):
+        time_oracle_pass(wl, shapes, inputs)
+    times = [time_oracle_pass(wl, shapes, inputs) for _ in range(args.steps)]
+    total = sum(times)
+    nbytes = sample_bytes(wl, shapes)
+    value = nbytes * args.steps / total / 1e9
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "num_ranks": wl.num_ranks, "num_params": wl.num_params,
+                   "psi": wl.psi, "sample": "bounded CPU sample, see cpu_baseline"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": describe_sample(wl, shapes),
+                         "host_cores": cpu_cores()},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_tide(args):
+    import torch
+
+    world, rank, local = dist_setup(args.gpus)
+    import layout_aware_collectives_gb300 as tide
+    import synth
+    from synth.device import DeviceJob
+
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    wl = synth.WORKLOADS[args.config]()
+    layout = tide.Layout(wl.shapes, wl.num_ranks)
+    job = DeviceJob(wl, layout, guard=False)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    gptr = tide.PointerTable(job.grad_ptrs())
+    sptr = tide.PointerTable(job.shard_ptrs())
+    pptr = tide.PointerTable(job.param_ptrs())
+    scale = wl.scale
+    rs_bytes, ag_bytes = wl.rs_bytes(), wl.ag_bytes()
+    small = (rs_bytes + ag_bytes) < 2 * L2_BYTES
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if small else None
+
+    def step():
+        layout.reduce_scatter(gptr, sptr, scale, stream)
+        layout.place(job.gathered, pptr, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(dev if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            if flush is not None:
+                flush.fill_(float(i))
+            ev[i][0].record(stream)
+            layout.reduce_scatter(gptr, sptr, scale, stream)
+            ev[i][1].record(stream)
+            layout.place(job.gathered, pptr, stream)
+            ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    clk = clocks.stop(t0, t1)
+    rs_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    ag_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    if flush is None:
+        step_ms_local = ev[0][0].elapsed_time(ev[K - 1][2]) / K
+    else:
+        step_ms_local = sum(r + a for r, a in zip(rs_ms, ag_ms)) / K
+    step_ms = reduce_max(step_ms_local, world)
+    value = world * (rs_bytes + ag_bytes) / (step_ms * 1e-3) / 1e9
+    rs_avg = statistics.mean(rs_ms)
+    ag_avg = statistics.mean(ag_ms)
+
+    peak, peak_src = measured_peaks()
+    rs_gbs = rs_bytes / (rs_avg * 1e-3) / 1e9
+    ag_gbs = ag_bytes / (ag_avg * 1e-3) / 1e9
+    grid_rs, block_rs = layout.launch_shape(tide.TIDE_OP_RS)
+    grid_ag, block_ag = layout.launch_shape(tide.TIDE_OP_AG)
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->f32", "data": "synthetic",
+        "config": {"workload": wl.name, "num_ranks": wl.num_ranks, "num_params": wl.num_params,
+                   "psi": wl.psi, "rs_bytes": rs_bytes, "ag_bytes": ag_bytes,
+                   "l2": "flushed between steps" if small else
+                   f"inputs larger than L2 ({(rs_bytes + ag_bytes) / 1e9:.1f} GB per step)",
+                   "mode": "uncapped", "parallelism": f"replicas x{world}"},
+        "kernels": {
+            "rs": {"ms": round(rs_avg, 4), "GB/s": round(rs_gbs, 1), "frac": round(rs_gbs / peak, 4),
+                   "grid": grid_rs, "block": block_rs},
+            "ag": {"ms": round(ag_avg, 4), "GB/s": round(ag_gbs, 1), "frac": round(ag_gbs / peak, 4),
+                   "grid": grid_ag, "block": block_ag},
+        },
+        "roofline": {"bound": "hbm", "kernel": "tide rs_kernel", "achieved": round(rs_gbs, 1),
+                     "peak": peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": round(rs_gbs / peak, 4),
+                     "traffic": recorded_traffic(wl.name)},
+        "clocks": clk,
+        "gpu_launches": 2 * K,
+        "device": props.name,
+    }
+
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(tide, layout, job, wl, stream, K, world)
+    if not args.no_interference:
+        out["interference"] = run_interference(tide, layout, job, wl, props)
+    layout.set_mode(tide.TIDE_MODE_UNCAPPED)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, 10.0)
+    if rank == 0:
+        print(json.dumps(out))
+    layout.close()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(tide, layout, job, wl, stream, K, world):
+    """Same metric through the public API with HOST inputs and outputs: each
+    step copies the N*P gradients and the gathered buffer from pinned host
+    memory, runs both operations, and copies the shards and parameters back."""
+    import torch
+
+    flat_g = [g for row in job.grads for g in row]
+    flat_s = [s for row in job.shards for s in row]
+    h_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in flat_g]
+    h_s = [torch.empty(s.shape, dtype=s.dtype, pin_memory=True) for s in flat_s]
+    h_buf = torch.empty(job.gathered.shape, dtype=job.gathered.dtype, pin_memory=True)
+    h_p = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in job.params]
+    for h, d in zip(h_g, flat_g):
+        h.copy_(d)
+    h_buf.copy_(job.gathered)
+    torch.cuda.synchronize()
+    h2d = sum(h.numel() * h.element_size() for h in h_g) + h_buf.numel() * 2
+    d2h = sum(h.numel() * h.element_size() for h in h_s) + sum(h.numel() * 2 for h in h_p)
+    gptr = tide.PointerTable(job.grad_ptrs())
+    sptr = tide.PointerTable(job.shard_ptrs())
+    pptr = tide.PointerTable(job.param_ptrs())
+    steps = max(3, min(K, 20))
+
+    def one():
+        for d, h in zip(flat_g, h_g):
+            d.copy_(h, non_blocking=True)
+        job.gathered.copy_(h_buf, non_blocking=True)
+        layout.reduce_scatter(gptr, sptr, wl.scale, stream)
+        layout.place(job.gathered, pptr, stream)
+        for h, d in zip(h_s, flat_s):
+            h.copy_(d, non_blocking=True)
+        for h, d in zip(h_p, job.params):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = reduce_max(e0.elapsed_time(e1) / steps, world)
+    val = world * (wl.rs_bytes() + wl.ag_bytes()) / (ms * 1e-3) / 1e9
+    del h_g, h_s, h_buf, h_p
+    return {"value": round(val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": steps}
+
+
+def run_interference(tide, layout, job, wl, props):
+    """Slowdown of a bf16 8192^3 GEMM on one stream while the reduce-scatter
+    (or placement) loops on another, per mode; SM.time of each mode."""
+    import torch
+
+    n = 8192
+    a = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    b = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    c = torch.empty(n, n, dtype=torch.bfloat16, device="cuda")
+    sg = torch.cuda.Stream()
+    sr = torch.cuda.Stream()
+    gptr = tide.PointerTable(job.grad_ptrs())
+    sptr = tide.PointerTable(job.shard_ptrs())
+    pptr = tide.PointerTable(job.param_ptrs())
+    reps = 8
+
+    def gemm_ms():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(sg):
+            e0.record(sg)
+            for _ in range(reps):
+                torch.matmul(a, b, out=c)
+            e1.record(sg)
+        return e0, e1
+
+    def op_ms(op, count=3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(sr)
+        for _ in range(count):
+            op()
+        e1.record(sr)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / count
+
+    # GEMM alone
+    for _ in range(3):
+        gemm_ms()
+    torch.cuda.synchronize()
+    alone = []
+    for _ in range(5):
+        e0, e1 = gemm_ms()
+        torch.cuda.synchronize()
+        alone.append(e0.elapsed_time(e1) / reps)
+    t0 = statistics.median(alone)
+    flops = 2 * n ** 3
+    res = {"gemm": f"bf16 {n}x{n}x{n} torch.matmul", "gemm_ms_alone": round(t0, 4),
+           "gemm_tflops_alone": round(flops / (t0 * 1e-3) / 1e12, 1), "modes": []}
+    modes = [("rs", "uncapped", tide.TIDE_MODE_UNCAPPED, 0)]
+    modes += [("rs", f"capped{cap}", tide.TIDE_MODE_CAPPED, cap) for cap in (8, 16, 32, 64)]
+    modes += [("ag", "uncapped", tide.TIDE_MODE_UNCAPPED, 0),
+              ("ag", "copy_engine", tide.TIDE_MODE_COPY_ENGINE, 0)]
+    for kind, name, mode, cap in modes:
+        layout.set_mode(mode, cap)
+        if kind == "rs":
+            def op():
+                layout.reduce_scatter(gptr, sptr, wl.scale, sr)
+            nbytes = wl.rs_bytes()
+            opname = tide.TIDE_OP_RS
+        else:
+            def op():
+                layout.place(job.gathered, pptr, sr)
+            nbytes = wl.ag_bytes()
+            opname = tide.TIDE_OP_AG
+        with torch.cuda.stream(sr):
+            op()
+            alone_ms = op_ms(op)
+            # enough launches to cover the GEMM window twice over
+            count = max(2, int(2 * reps * t0 / max(alone_ms, 1e-3)) + 2)
+            torch.cuda.synchronize()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(sr)
+            for _ in range(count):
+                op()
+            s1.record(sr)
+        # start the GEMMs once the reduce-scatter loop is running
+        time.sleep(0.002)
+        e0, e1 = gemm_ms()
+        torch.cuda.synchronize()
+        t1 = e0.elapsed_time(e1) / reps
+        loop_ms = s0.elapsed_time(s1) / count
+        grid, _ = layout.launch_shape(opname)
+        sm_used = min(grid, props.multi_processor_count) if grid else 0
+        res["modes"].append({
+            "op": kind, "mode": name, "grid": grid,
+            "op_ms_alone": round(alone_ms, 4),
+            "op_GB/s_alone": round(nbytes / (alone_ms * 1e-3) / 1e9, 1),
+            "op_ms_concurrent": round(loop_ms, 4),
+            "gemm_ms_concurrent": round(t1, 4),
+            "gemm_slowdown_pct": round(100.0 * (t1 / t0 - 1.0), 2),
+            "sm_ms": round(alone_ms * sm_used, 2),
+        })
+    del a, b, c
+    return res
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_tide(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

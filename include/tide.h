@@ -1,0 +1,212 @@
+/*
+ * tide.h — C ABI of libtide.so: layout-aware reduce-scatter math and
+ * all-gather placement for FSDP2-style per-parameter storage, on one GPU
+ * (sm_103a), with N data-parallel ranks simulated by N input/output sets.
+ *
+ * What the operations are (sources cited by page title and section):
+ *
+ *  - "FSDP通信终局：TIDE零拷贝集合通信优化" §FSDP2通信开销的根源: FSDP2 keeps
+ *    parameters and gradients as one tensor per parameter, while its
+ *    collectives work on flat rank-major buffers (each rank's elements
+ *    contiguous, rank blocks one after another).  The all-gather output
+ *    therefore has to be copied into parameter storage and gradients packed
+ *    into a full fp32 buffer.  Reduce-scatter: every rank holds a full
+ *    buffer; afterwards each rank holds one reduced shard.
+ *  - same page, §TIDE的设计思路: TIDE-RS consumes the per-parameter bf16
+ *    gradients directly and reduces them into fp32 shards (a mixed-precision
+ *    mode NCCL lacks); TIDE-AG delivers shards straight into parameter
+ *    storage, folding the placement into the collective's addressing.
+ *    Intra-node accumulation uses copy engines and short-lived CTAs.
+ *
+ * This library computes, on one GPU, the data path of both: the reduction
+ * math of TIDE-RS written straight into each rank's padded fp32 dim-0 shard
+ * of every parameter (no flat pack buffer), and the placement of a
+ * rank-major bf16 buffer straight into per-parameter storage (no copy-out).
+ *
+ * Sharding (FSDP2's dim-0 rule; the pages do not spell it out): parameter p
+ * of shape [d0, ...] is viewed as a row-major [d0, inner] matrix
+ * (inner = product of the trailing dims, 1 for a 1-D tensor, and a 0-dim
+ * scalar is [1]).  With c = ceil(d0 / N), rank r owns rows
+ * [r*c, min((r+1)*c, d0)) and its shard is padded with zero rows to c rows
+ * (c * inner elements).  Ranks past the end own no rows (all padding).
+ *
+ * Rank-major buffer: N blocks of S elements; inside each block parameter
+ * p's shard starts at offset o_p, o_0 = 0,
+ * o_{p+1} = roundup(o_p + c_p * inner_p, A), S = roundup(o_P, A), A the
+ * alignment in elements (8 by default: every shard starts on 16 bytes).
+ *
+ * Conventions for every call:
+ *  - All device pointers are CUDA device pointers of the device that is
+ *    current when the layout is first used; tables of pointers are HOST
+ *    arrays read only during the call.  The caller owns every device buffer
+ *    and keeps it alive until the work enqueued on `stream` completes.
+ *  - Compute calls are asynchronous with respect to the host and never
+ *    synchronise the device.  The first compute call of a layout uploads its
+ *    tables to the device (allocating them); make one call before capturing
+ *    a stream into a CUDA graph.
+ *  - A layout may be used from several host threads (calls are serialised
+ *    internally).  Calls on different streams that write the same output
+ *    buffers race, as any two kernels would.
+ *  - Errors: TIDE_ERR_INVALID_ARG for null / out-of-range / overflowing
+ *    arguments, TIDE_ERR_MISALIGNED for a pointer that is not 16-byte
+ *    aligned (a null pointer for a zero-size tensor is accepted),
+ *    TIDE_ERR_UNSUPPORTED for a mode that an operation does not have,
+ *    TIDE_ERR_CUDA when the CUDA runtime reports an error (the message is
+ *    kept per host thread, see tide_last_error()).  On any error nothing is
+ *    enqueued on the stream.
+ */
+#ifndef TIDE_H
+#define TIDE_H
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define TIDE_API __attribute__((visibility("default")))
+#else
+#define TIDE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TIDE_OK = 0,
+  TIDE_ERR_INVALID_ARG = 1,
+  TIDE_ERR_MISALIGNED = 2,
+  TIDE_ERR_UNSUPPORTED = 3,
+  TIDE_ERR_CUDA = 4,
+  TIDE_ERR_TIMEOUT = 5, /* reserved for bounded device-side waits */
+  TIDE_ERR_OUT_OF_MEMORY = 6
+} tide_status_t;
+
+typedef enum {
+  /* Kernels launched over the whole GPU (grid sized by occupancy x SMs). */
+  TIDE_MODE_UNCAPPED = 0,
+  /* Persistent kernels with at most `cta_cap` CTAs looping over the tile
+   * list: the short-lived-CTA budget of "TIDE的设计思路", trading bandwidth
+   * for SM time left to concurrent compute. */
+  TIDE_MODE_CAPPED = 1,
+  /* Placement through the copy engines (cudaMemcpy2DAsync, no SM use), the
+   * copy-engine path of "TIDE的设计思路".  Reduce-scatter has no copy-engine
+   * form: it returns TIDE_ERR_UNSUPPORTED in this mode. */
+  TIDE_MODE_COPY_ENGINE = 2
+} tide_mode_t;
+
+typedef enum { TIDE_OP_RS = 0, TIDE_OP_AG = 1 } tide_op_t;
+
+/* Maximum simulated ranks per layout. */
+#define TIDE_MAX_RANKS 4096
+
+typedef struct tide_layout_s* tide_layout_t;
+
+/*
+ * Create the layout descriptor of `num_params` parameters sharded over
+ * `num_ranks` ranks (host-only; no CUDA call is made).
+ *   ndims[p]    number of dims of parameter p (0 = scalar, treated as [1]);
+ *   dims_flat   all dims back to back (sum of ndims entries), each >= 0;
+ *   num_ranks   1 .. TIDE_MAX_RANKS;
+ *   out         receives the handle (owned by the caller, free with
+ *               tide_layout_destroy).
+ * Parameter order inside a rank block is the order given.  num_params == 0
+ * gives an empty layout whose calls do nothing.  Alignment A = 8 elements.
+ */
+TIDE_API tide_status_t tide_layout_create(int32_t num_params, const int32_t* ndims,
+                                 const int64_t* dims_flat, int32_t num_ranks,
+                                 tide_layout_t* out);
+
+/* As tide_layout_create with an explicit offset alignment `align_elems`
+ * (1, 2, 4, 8, 16, ... elements; a power of two <= 4096).  With A < 8 rank
+ * slices may start off 16 bytes; such tiles take a scalar path. */
+TIDE_API tide_status_t tide_layout_create_ex(int32_t num_params, const int32_t* ndims,
+                                    const int64_t* dims_flat, int32_t num_ranks,
+                                    int64_t align_elems, tide_layout_t* out);
+
+/* Free the layout and every host/device resource it owns.  Work already
+ * enqueued that uses the layout's device tables must have completed.
+ * Passing NULL does nothing. */
+TIDE_API void tide_layout_destroy(tide_layout_t layout);
+
+/* Queries (host-only).  Indices out of range give TIDE_ERR_INVALID_ARG. */
+TIDE_API tide_status_t tide_layout_num_params(tide_layout_t layout, int32_t* num_params);
+TIDE_API tide_status_t tide_layout_num_ranks(tide_layout_t layout, int32_t* num_ranks);
+/* S: elements of one rank block of the gathered buffer (the buffer holds
+ * num_ranks * S bf16 elements). */
+TIDE_API tide_status_t tide_layout_rank_block_numel(tide_layout_t layout, int64_t* block_numel);
+/* c_p * inner_p: elements of each fp32 shard of parameter p. */
+TIDE_API tide_status_t tide_layout_shard_numel(tide_layout_t layout, int32_t p, int64_t* numel);
+/* o_p: offset of parameter p's shard inside every rank block. */
+TIDE_API tide_status_t tide_layout_param_offset(tide_layout_t layout, int32_t p, int64_t* offset);
+/* Rows of parameter p that rank r really owns (the rest of its shard is padding). */
+TIDE_API tide_status_t tide_layout_valid_rows(tide_layout_t layout, int32_t p, int32_t r, int64_t* rows);
+/* c_p = ceil(d0_p / N). */
+TIDE_API tide_status_t tide_layout_chunk_rows(tide_layout_t layout, int32_t p, int64_t* rows);
+
+/* Select how the compute calls run (default TIDE_MODE_UNCAPPED).  cta_cap is
+ * read in TIDE_MODE_CAPPED only and must be >= 1. */
+TIDE_API tide_status_t tide_layout_set_mode(tide_layout_t layout, tide_mode_t mode, int32_t cta_cap);
+
+/* Grid and block size the next launch of `op` will use under the current
+ * mode, for the device that is current (grid 0 means no kernel: an empty
+ * layout, or copy-engine placement).  Host-only until the first compute
+ * call; uses the current device's SM count. */
+TIDE_API tide_status_t tide_layout_launch_shape(tide_layout_t layout, tide_op_t op, int32_t* grid,
+                                       int32_t* block);
+
+/* Work list of `op` as rows of 6 int64 (param, rank, src_offset,
+ * dst_offset, length, flags) into `rows` (capacity `cap` rows); *count gets
+ * the number of tiles.  Host-only; for tests and tools. */
+TIDE_API tide_status_t tide_layout_tiles(tide_layout_t layout, tide_op_t op, int64_t* rows, int64_t cap,
+                                int64_t* count);
+
+/*
+ * Reduce-scatter math of TIDE-RS ("TIDE的设计思路"): for every rank r,
+ * parameter p, shard row i' < c_p and column j, with i = r*c_p + i',
+ *   shards[r*P + p][i'*inner_p + j] =
+ *       scale * sum_{k=0}^{N-1} f32(grads[k*P + p][i*inner_p + j])   if i < d0_p
+ *       +0.0f                                                       otherwise,
+ * the sum taken in fp32 in ascending k from +0.0f, every add and the final
+ * multiply rounded to nearest even, subnormals kept.
+ *   grads   host array of N*P device pointers, rank-major: grads[k*P + p]
+ *           is rank k's bf16 gradient of parameter p (d0_p*inner_p
+ *           elements, contiguous row-major, 16-byte aligned);
+ *   shards  host array of N*P device pointers: shards[r*P + p] is rank r's
+ *           fp32 shard of parameter p (c_p*inner_p elements, 16-byte
+ *           aligned); every element, padding included, is written;
+ *   scale   applied after the sum (1/N averages);
+ *   stream  CUDA stream the kernel is enqueued on.
+ * Outputs must not overlap inputs or each other.  In TIDE_MODE_COPY_ENGINE
+ * returns TIDE_ERR_UNSUPPORTED.
+ */
+TIDE_API tide_status_t tide_rs_bf16_to_fp32(tide_layout_t layout, const uint16_t* const* grads,
+                                   float* const* shards, float scale, cudaStream_t stream);
+
+/*
+ * Placement of TIDE-AG ("TIDE的设计思路"; rank-major buffer of
+ * "FSDP2通信开销的根源"): for every parameter p, row i < d0_p and column j,
+ * with r = i / c_p,
+ *   params[p][i*inner_p + j] = gathered[r*S + o_p + (i - r*c_p)*inner_p + j].
+ * Padding and alignment slots of `gathered` are never read.
+ *   gathered  device pointer to N*S bf16 elements (16-byte aligned);
+ *   params    host array of P device pointers, params[p] is parameter p's
+ *             bf16 storage (d0_p*inner_p elements, 16-byte aligned);
+ *   stream    CUDA stream the work is enqueued on (a kernel, or copy-engine
+ *             copies in TIDE_MODE_COPY_ENGINE).
+ * A bit copy: the result is bit-exact.  Outputs must not overlap the input.
+ */
+TIDE_API tide_status_t tide_ag_place(tide_layout_t layout, const uint16_t* gathered,
+                            uint16_t* const* params, cudaStream_t stream);
+
+/* Static description of a status code. */
+TIDE_API const char* tide_status_string(tide_status_t status);
+
+/* Message of the last failed call on this host thread ("" if none). */
+TIDE_API const char* tide_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TIDE_H */

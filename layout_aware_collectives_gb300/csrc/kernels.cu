@@ -1,0 +1,240 @@
+// Reduce-scatter math and all-gather placement kernels for sm_103a.
+//
+// Both are HBM-streaming kernels: the reduce-scatter reads N bf16 values and
+// writes one fp32 value per element (about one fp32 add per 2 bytes read),
+// the placement is a segmented bit copy.  Neither is a dense contraction, so
+// there is no tensor-core path; what matters is 16-byte coalesced accesses,
+// enough bytes in flight per SM and a flat tile list that balances many
+// small tensors.
+//
+// Sources: "FSDP通信终局：TIDE零拷贝集合通信优化" §TIDE的设计思路 (TIDE-RS:
+// per-parameter bf16 gradients reduced straight into fp32 shards; TIDE-AG:
+// shards delivered straight into parameter storage; short-lived CTAs) and
+// §FSDP2通信开销的根源 (rank-major buffers, reduce-scatter semantics).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tide_internal.h"
+
+namespace tide {
+namespace {
+
+// ---------------------------------------------------------------- memory ops
+// Streaming 16-byte load of data that is read exactly once: read-only path,
+// no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t* p) {
+  uint16_t r;
+  asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+
+// Streaming (evict-first) stores: outputs are not re-read by this kernel.
+__device__ __forceinline__ void st_stream(float* p, float a, float b, float c, float d) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// bf16 -> fp32 is exact: a bf16 is the upper half of an fp32 word.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// acc[0..7] += the 8 bf16 values packed in v (in element order).
+__device__ __forceinline__ void add8(float (&acc)[8], const uint4& v) {
+  acc[0] = __fadd_rn(acc[0], bf16_lo(v.x));
+  acc[1] = __fadd_rn(acc[1], bf16_hi(v.x));
+  acc[2] = __fadd_rn(acc[2], bf16_lo(v.y));
+  acc[3] = __fadd_rn(acc[3], bf16_hi(v.y));
+  acc[4] = __fadd_rn(acc[4], bf16_lo(v.z));
+  acc[5] = __fadd_rn(acc[5], bf16_hi(v.z));
+  acc[6] = __fadd_rn(acc[6], bf16_lo(v.w));
+  acc[7] = __fadd_rn(acc[7], bf16_hi(v.w));
+}
+
+// ---------------------------------------------------------------- reduce-scatter
+// One group of G ranks starting at rank k0: issue all G*V loads, then add
+// them in ascending rank order.  FULL means k0 + G <= N is known.
+template <int G, int V, bool FULL>
+__device__ __forceinline__ void rs_group(float (&acc)[V][8], const uint16_t* const* s_src, int k0,
+                                         int n, int v0, int nvec) {
+  uint4 d[G][V];
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+#pragma unroll
+    for (int u = 0; u < V; ++u)
+      if ((FULL || k0 + j < n) && v0 + u * (int)blockDim.x < nvec)
+        d[j][u] = ld_stream(s_src[k0 + j] + 8 * (v0 + u * (int)blockDim.x));
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+    if (FULL || k0 + j < n)
+#pragma unroll
+      for (int u = 0; u < V; ++u) add8(acc[u], d[j][u]);
+}
+
+// One tile = a run of `len` elements of parameter p that lands in rank r's
+// shard.  Every rank k contributes the element at the same offset of its own
+// gradient (the shard rows are the same rows in every rank's full gradient),
+// so the tile reads N equally-long contiguous runs and writes one.
+//
+// Each thread owns V 8-element vectors per pass.  Loads are issued in
+// groups of G ranks (all G*V 16-byte loads before any add) and the adds run
+// in ascending rank order, so the fp32 result equals the sequential sum
+// acc = ((0 + g_0) + g_1) + ... + g_{N-1}, then one multiply by the scale.
+// NFIX > 0 fixes N at compile time (full unroll, no predicates).
+template <int NFIX, int G, int V>
+__global__ void __launch_bounds__(kRsThreads) rs_kernel(RsArgs a) {
+  extern __shared__ const uint16_t* s_src[];  // the current tile's N source pointers
+  const int N = NFIX > 0 ? NFIX : a.num_ranks;
+  for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+    const Tile tile = a.tiles[t];
+    float* __restrict__ out = a.stab[(int64_t)tile.r * a.num_params + tile.p] + tile.dst;
+
+    if (tile.flags & kTileZero) {  // padding rows of the shard
+      if (tile.flags & kTileVec) {
+        const int nv = tile.len >> 2;
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) st_stream(out + 4 * i, 0.f, 0.f, 0.f, 0.f);
+        for (int e = 4 * nv + threadIdx.x; e < tile.len; e += blockDim.x) out[e] = 0.f;
+      } else {
+        for (int e = threadIdx.x; e < tile.len; e += blockDim.x) out[e] = 0.f;
+      }
+      continue;
+    }
+
+    __syncthreads();  // every thread is done with the previous tile's pointers
+    for (int k = threadIdx.x; k < N; k += blockDim.x)
+      s_src[k] = a.gtab[(int64_t)tile.p * N + k] + tile.src;
+    __syncthreads();
+
+    if (tile.flags & kTileVec) {
+      const int nvec = tile.len >> 3;
+      for (int v0 = threadIdx.x; v0 < nvec; v0 += V * blockDim.x) {
+        float acc[V][8];
+#pragma unroll
+        for (int u = 0; u < V; ++u)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+        if constexpr (NFIX > 0) {
+#pragma unroll
+          for (int k0 = 0; k0 < NFIX; k0 += G) rs_group<G, V, true>(acc, s_src, k0, N, v0, nvec);
+        } else {
+          for (int k0 = 0; k0 < N; k0 += G) rs_group<G, V, false>(acc, s_src, k0, N, v0, nvec);
+        }
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          const int v = v0 + u * blockDim.x;
+          if (v < nvec) {
+            float* o = out + 8 * v;
+            st_stream(o, __fmul_rn(acc[u][0], a.scale), __fmul_rn(acc[u][1], a.scale),
+                      __fmul_rn(acc[u][2], a.scale), __fmul_rn(acc[u][3], a.scale));
+            st_stream(o + 4, __fmul_rn(acc[u][4], a.scale), __fmul_rn(acc[u][5], a.scale),
+                      __fmul_rn(acc[u][6], a.scale), __fmul_rn(acc[u][7], a.scale));
+          }
+        }
+      }
+      for (int e = 8 * nvec + threadIdx.x; e < tile.len; e += blockDim.x) {
+        float acc = 0.f;
+        for (int k = 0; k < N; ++k) acc = __fadd_rn(acc, bf16_f32(ld_stream_u16(s_src[k] + e)));
+        out[e] = __fmul_rn(acc, a.scale);
+      }
+    } else {  // a run whose source is not 16-byte aligned: element by element
+      for (int e = threadIdx.x; e < tile.len; e += blockDim.x) {
+        float acc = 0.f;
+        for (int k = 0; k < N; ++k) acc = __fadd_rn(acc, bf16_f32(ld_stream_u16(s_src[k] + e)));
+        out[e] = __fmul_rn(acc, a.scale);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- placement
+// One tile = a contiguous run of rank r's chunk of parameter p: a copy from
+// gathered[r*S + o_p + ...] to params[p][r*c_p*inner_p + ...].  U 16-byte
+// vectors per thread are loaded before any is stored.
+template <int U>
+__global__ void __launch_bounds__(kAgThreads) ag_kernel(AgArgs a) {
+  for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+    const Tile tile = a.tiles[t];
+    const uint16_t* __restrict__ src = a.buf + tile.src;
+    uint16_t* __restrict__ dst = a.ptab[tile.p] + tile.dst;
+    if (tile.flags & kTileVec) {
+      const int nvec = tile.len >> 3;
+      for (int v0 = threadIdx.x; v0 < nvec; v0 += U * blockDim.x) {
+        uint4 d[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (v0 + u * (int)blockDim.x < nvec) d[u] = ld_stream(src + 8 * (v0 + u * blockDim.x));
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (v0 + u * (int)blockDim.x < nvec) st_stream(dst + 8 * (v0 + u * blockDim.x), d[u]);
+      }
+      for (int e = 8 * nvec + threadIdx.x; e < tile.len; e += blockDim.x) dst[e] = ld_stream_u16(src + e);
+    } else {
+      for (int e = threadIdx.x; e < tile.len; e += blockDim.x) dst[e] = ld_stream_u16(src + e);
+    }
+  }
+}
+
+constexpr int kAgUnroll = 4;
+
+// ---------------------------------------------------------------- dispatch
+using RsKernel = void (*)(RsArgs);
+
+RsKernel rs_kernel_for(int32_t n) {
+  switch (n) {
+    case 1: return rs_kernel<1, 1, 8>;
+    case 2: return rs_kernel<2, 2, 4>;
+    case 3: return rs_kernel<3, 3, 2>;
+    case 4: return rs_kernel<4, 4, 2>;
+    case 5: return rs_kernel<5, 5, 1>;
+    case 6: return rs_kernel<6, 6, 1>;
+    case 7: return rs_kernel<7, 7, 1>;
+    case 8: return rs_kernel<8, 8, 1>;
+    case 16: return rs_kernel<16, 8, 1>;
+    case 32: return rs_kernel<32, 8, 1>;
+    case 64: return rs_kernel<64, 8, 1>;
+    default: return rs_kernel<0, 8, 1>;
+  }
+}
+
+}  // namespace
+
+size_t rs_smem_bytes(int32_t num_ranks) { return sizeof(const uint16_t*) * (size_t)num_ranks; }
+
+cudaError_t launch_rs(const RsArgs& a, int grid, cudaStream_t stream) {
+  if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
+  rs_kernel_for(a.num_ranks)<<<grid, kRsThreads, rs_smem_bytes(a.num_ranks), stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ag(const AgArgs& a, int grid, cudaStream_t stream) {
+  if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
+  ag_kernel<kAgUnroll><<<grid, kAgThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t rs_occupancy(int32_t num_ranks, int* blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, rs_kernel_for(num_ranks),
+                                                       kRsThreads, rs_smem_bytes(num_ranks));
+}
+
+cudaError_t ag_occupancy(int* blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, ag_kernel<kAgUnroll>,
+                                                       kAgThreads, 0);
+}
+
+}  // namespace tide

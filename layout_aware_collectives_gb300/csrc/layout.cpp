@@ -1,0 +1,275 @@
+// Host layout descriptor: per-parameter chunk / pad / offset tables and the
+// tile work lists of the reduce-scatter and placement kernels.  Host-only:
+// nothing here calls CUDA, so layouts can be built and inspected without a
+// GPU.  Device copies are made lazily by tide_api.cpp.
+//
+// Sharding follows FSDP2's dim-0 rule (c = ceil(d0 / N) rows per rank,
+// zero-padded); the rank-major block layout follows
+// "FSDP通信终局：TIDE零拷贝集合通信优化" §FSDP2通信开销的根源.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <algorithm>
+#include <new>
+
+#include "tide_internal.h"
+
+namespace tide {
+
+namespace {
+thread_local std::string g_last_error;
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
+bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow(a, b, out); }
+
+int64_t roundup(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Elements per reduce-scatter tile: about 256 KiB of bf16 reads across the N
+// ranks, at least one full CTA pass (256 threads x 8 elements).
+int64_t rs_tile_elems(int32_t n) {
+  int64_t t = (int64_t)131072 / n;
+  t = std::max<int64_t>(2048, std::min<int64_t>(65536, t));
+  return t / 8 * 8;
+}
+constexpr int64_t kAgTileElems = 32768;    // 64 KiB read + 64 KiB written
+constexpr int64_t kZeroTileElems = 65536;  // padding fill
+
+// Split [0, n) into near-equal runs of at most `t` elements, each run but
+// the last a multiple of 8 elements.
+template <typename F>
+void split_runs(int64_t n, int64_t t, F&& emit) {
+  if (n <= 0) return;
+  const int64_t pieces = (n + t - 1) / t;
+  const int64_t step = roundup((n + pieces - 1) / pieces, 8);
+  for (int64_t s = 0; s < n; s += step) emit(s, std::min(step, n - s));
+}
+
+void build_tiles(tide_layout_s* l) {
+  const int32_t N = l->num_ranks;
+  const int64_t T = rs_tile_elems(N);
+  l->rs_tiles.clear();
+  l->ag_tiles.clear();
+  for (int32_t p = 0; p < l->num_params; ++p) {
+    const int64_t c = l->chunk[p], inner = l->inner[p], d0 = l->d0[p];
+    for (int32_t r = 0; r < N; ++r) {
+      const int64_t v = std::max<int64_t>(0, std::min<int64_t>(c, d0 - (int64_t)r * c));
+      const int64_t seg = v * inner;
+      const int64_t rs_src = (int64_t)r * c * inner;
+      split_runs(seg, T, [&](int64_t s, int64_t n) {
+        Tile t{rs_src + s, s, (int32_t)n, p, r, 0u};
+        if (t.src % 8 == 0 && t.dst % 4 == 0) t.flags |= kTileVec;
+        l->rs_tiles.push_back(t);
+      });
+      split_runs(c * inner - seg, kZeroTileElems, [&](int64_t s, int64_t n) {
+        Tile t{0, seg + s, (int32_t)n, p, r, kTileZero};
+        if (t.dst % 4 == 0) t.flags |= kTileVec;
+        l->rs_tiles.push_back(t);
+      });
+      const int64_t ag_src = (int64_t)r * l->block_numel + l->offset[p];
+      split_runs(seg, kAgTileElems, [&](int64_t s, int64_t n) {
+        Tile t{ag_src + s, rs_src + s, (int32_t)n, p, r, 0u};
+        if (t.src % 8 == 0 && t.dst % 8 == 0) t.flags |= kTileVec;
+        l->ag_tiles.push_back(t);
+      });
+    }
+  }
+}
+
+tide_status_t create(int32_t num_params, const int32_t* ndims, const int64_t* dims_flat,
+                     int32_t num_ranks, int64_t align, tide_layout_t* out) {
+  if (!out) return set_error(TIDE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (num_params < 0) return set_error(TIDE_ERR_INVALID_ARG, "num_params < 0");
+  if (num_ranks < 1 || num_ranks > TIDE_MAX_RANKS)
+    return set_error(TIDE_ERR_INVALID_ARG, "num_ranks out of range 1..TIDE_MAX_RANKS");
+  if (align < 1 || align > 4096 || (align & (align - 1)))
+    return set_error(TIDE_ERR_INVALID_ARG, "align_elems must be a power of two in 1..4096");
+  if (num_params > 0 && !ndims) return set_error(TIDE_ERR_INVALID_ARG, "ndims is NULL");
+
+  tide_layout_s* l = new (std::nothrow) tide_layout_s();
+  if (!l) return set_error(TIDE_ERR_OUT_OF_MEMORY, "host allocation failed");
+  l->num_ranks = num_ranks;
+  l->num_params = num_params;
+  l->align = align;
+  int64_t pos = 0, o = 0, psi = 0;
+  for (int32_t p = 0; p < num_params; ++p) {
+    const int32_t nd = ndims[p];
+    if (nd < 0 || nd > 64) {
+      delete l;
+      return set_error(TIDE_ERR_INVALID_ARG, "ndims[" + std::to_string(p) + "] out of range");
+    }
+    if (nd > 0 && !dims_flat) {
+      delete l;
+      return set_error(TIDE_ERR_INVALID_ARG, "dims_flat is NULL");
+    }
+    int64_t d0 = 1, inner = 1;
+    for (int32_t d = 0; d < nd; ++d) {
+      const int64_t v = dims_flat[pos + d];
+      if (v < 0) {
+        delete l;
+        return set_error(TIDE_ERR_INVALID_ARG, "negative dim in parameter " + std::to_string(p));
+      }
+      if (d == 0) {
+        d0 = v;
+      } else if (!mul_ok(inner, v, &inner)) {
+        delete l;
+        return set_error(TIDE_ERR_INVALID_ARG, "size overflow in parameter " + std::to_string(p));
+      }
+    }
+    pos += nd;
+    int64_t numel = 0, shard = 0;
+    const int64_t c = (d0 + num_ranks - 1) / num_ranks;
+    if (!mul_ok(d0, inner, &numel) || !mul_ok(c, inner, &shard) || !add_ok(psi, numel, &psi) ||
+        !add_ok(o, shard, &o) || o > INT64_MAX / 2 || numel > INT64_MAX / 8) {
+      delete l;
+      return set_error(TIDE_ERR_INVALID_ARG, "size overflow in parameter " + std::to_string(p));
+    }
+    l->d0.push_back(d0);
+    l->inner.push_back(inner);
+    l->chunk.push_back(c);
+    l->shard_numel.push_back(shard);
+    l->offset.push_back(o - shard);
+    o = roundup(o, align);
+  }
+  l->block_numel = roundup(o, align);
+  int64_t total = 0;
+  if (!mul_ok(l->block_numel, num_ranks, &total) || total > INT64_MAX / 8) {
+    delete l;
+    return set_error(TIDE_ERR_INVALID_ARG, "gathered buffer size overflows");
+  }
+  try {
+    build_tiles(l);
+  } catch (const std::bad_alloc&) {
+    delete l;
+    return set_error(TIDE_ERR_OUT_OF_MEMORY, "host allocation of the tile lists failed");
+  }
+  *out = l;
+  return TIDE_OK;
+}
+
+}  // namespace
+
+tide_status_t set_error(tide_status_t st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+tide_status_t cuda_fail(cudaError_t e, const char* what) {
+  std::string m = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return set_error(e == cudaErrorMemoryAllocation ? TIDE_ERR_OUT_OF_MEMORY : TIDE_ERR_CUDA, m);
+}
+
+}  // namespace tide
+
+using tide::set_error;
+
+extern "C" {
+
+tide_status_t tide_layout_create(int32_t num_params, const int32_t* ndims, const int64_t* dims_flat,
+                                 int32_t num_ranks, tide_layout_t* out) {
+  return tide::create(num_params, ndims, dims_flat, num_ranks, 8, out);
+}
+
+tide_status_t tide_layout_create_ex(int32_t num_params, const int32_t* ndims,
+                                    const int64_t* dims_flat, int32_t num_ranks,
+                                    int64_t align_elems, tide_layout_t* out) {
+  return tide::create(num_params, ndims, dims_flat, num_ranks, align_elems, out);
+}
+
+tide_status_t tide_layout_num_params(tide_layout_t l, int32_t* v) {
+  if (!l || !v) return set_error(TIDE_ERR_INVALID_ARG, "NULL argument");
+  *v = l->num_params;
+  return TIDE_OK;
+}
+
+tide_status_t tide_layout_num_ranks(tide_layout_t l, int32_t* v) {
+  if (!l || !v) return set_error(TIDE_ERR_INVALID_ARG, "NULL argument");
+  *v = l->num_ranks;
+  return TIDE_OK;
+}
+
+tide_status_t tide_layout_rank_block_numel(tide_layout_t l, int64_t* v) {
+  if (!l || !v) return set_error(TIDE_ERR_INVALID_ARG, "NULL argument");
+  *v = l->block_numel;
+  return TIDE_OK;
+}
+
+#define TIDE_CHECK_P(l, p, v)                                                   \
+  do {                                                                          \
+    if (!(l) || !(v)) return set_error(TIDE_ERR_INVALID_ARG, "NULL argument");  \
+    if ((p) < 0 || (p) >= (l)->num_params)                                      \
+      return set_error(TIDE_ERR_INVALID_ARG, "parameter index out of range");   \
+  } while (0)
+
+tide_status_t tide_layout_shard_numel(tide_layout_t l, int32_t p, int64_t* v) {
+  TIDE_CHECK_P(l, p, v);
+  *v = l->shard_numel[p];
+  return TIDE_OK;
+}
+
+tide_status_t tide_layout_param_offset(tide_layout_t l, int32_t p, int64_t* v) {
+  TIDE_CHECK_P(l, p, v);
+  *v = l->offset[p];
+  return TIDE_OK;
+}
+
+tide_status_t tide_layout_chunk_rows(tide_layout_t l, int32_t p, int64_t* v) {
+  TIDE_CHECK_P(l, p, v);
+  *v = l->chunk[p];
+  return TIDE_OK;
+}
+
+tide_status_t tide_layout_valid_rows(tide_layout_t l, int32_t p, int32_t r, int64_t* v) {
+  TIDE_CHECK_P(l, p, v);
+  if (r < 0 || r >= l->num_ranks) return set_error(TIDE_ERR_INVALID_ARG, "rank out of range");
+  const int64_t c = l->chunk[p];
+  *v = std::max<int64_t>(0, std::min<int64_t>(c, l->d0[p] - (int64_t)r * c));
+  return TIDE_OK;
+}
+
+tide_status_t tide_layout_set_mode(tide_layout_t l, tide_mode_t mode, int32_t cta_cap) {
+  if (!l) return set_error(TIDE_ERR_INVALID_ARG, "NULL layout");
+  if (mode != TIDE_MODE_UNCAPPED && mode != TIDE_MODE_CAPPED && mode != TIDE_MODE_COPY_ENGINE)
+    return set_error(TIDE_ERR_INVALID_ARG, "unknown mode");
+  if (mode == TIDE_MODE_CAPPED && cta_cap < 1)
+    return set_error(TIDE_ERR_INVALID_ARG, "cta_cap must be >= 1 in TIDE_MODE_CAPPED");
+  std::lock_guard<std::mutex> g(l->mu);
+  l->mode = mode;
+  l->cta_cap = mode == TIDE_MODE_CAPPED ? cta_cap : 0;
+  return TIDE_OK;
+}
+
+tide_status_t tide_layout_tiles(tide_layout_t l, tide_op_t op, int64_t* rows, int64_t cap,
+                                int64_t* count) {
+  if (!l || !count) return set_error(TIDE_ERR_INVALID_ARG, "NULL argument");
+  if (op != TIDE_OP_RS && op != TIDE_OP_AG) return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
+  const std::vector<tide::Tile>& t = op == TIDE_OP_RS ? l->rs_tiles : l->ag_tiles;
+  *count = (int64_t)t.size();
+  if (cap > 0 && !rows) return set_error(TIDE_ERR_INVALID_ARG, "rows is NULL");
+  for (int64_t i = 0; i < std::min<int64_t>(cap, (int64_t)t.size()); ++i) {
+    rows[6 * i + 0] = t[i].p;
+    rows[6 * i + 1] = t[i].r;
+    rows[6 * i + 2] = t[i].src;
+    rows[6 * i + 3] = t[i].dst;
+    rows[6 * i + 4] = t[i].len;
+    rows[6 * i + 5] = t[i].flags;
+  }
+  return TIDE_OK;
+}
+
+const char* tide_status_string(tide_status_t s) {
+  switch (s) {
+    case TIDE_OK: return "TIDE_OK";
+    case TIDE_ERR_INVALID_ARG: return "TIDE_ERR_INVALID_ARG: invalid argument";
+    case TIDE_ERR_MISALIGNED: return "TIDE_ERR_MISALIGNED: pointer not 16-byte aligned";
+    case TIDE_ERR_UNSUPPORTED: return "TIDE_ERR_UNSUPPORTED: operation not available in this mode";
+    case TIDE_ERR_CUDA: return "TIDE_ERR_CUDA: CUDA runtime error";
+    case TIDE_ERR_TIMEOUT: return "TIDE_ERR_TIMEOUT: bounded device wait expired";
+    case TIDE_ERR_OUT_OF_MEMORY: return "TIDE_ERR_OUT_OF_MEMORY: allocation failed";
+  }
+  return "unknown tide_status_t";
+}
+
+const char* tide_last_error(void) { return tide::g_last_error.c_str(); }
+
+}  // extern "C"

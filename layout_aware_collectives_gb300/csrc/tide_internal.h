@@ -1,0 +1,106 @@
+// Internal interface between the host layout descriptor / C ABI
+// (layout.cpp, tide_api.cpp) and the CUDA kernels (kernels.cu).
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "tide.h"
+
+namespace tide {
+
+// One unit of kernel work: a contiguous run of `len` elements of one
+// (parameter, rank) segment.  32 bytes, read once per tile by every CTA.
+struct Tile {
+  int64_t src;     // RS: element offset into grads[k][p] (same for every k)
+                   // AG: element offset into the gathered buffer
+  int64_t dst;     // RS: element offset into shards[r][p]; AG: into params[p]
+  int32_t len;     // elements
+  int32_t p;       // parameter
+  int32_t r;       // rank whose shard / chunk the run belongs to
+  uint32_t flags;  // kTileZero | kTileVec
+};
+static_assert(sizeof(Tile) == 32, "Tile is 32 bytes");
+
+constexpr uint32_t kTileZero = 1u;  // RS only: write +0.0f (padding rows)
+constexpr uint32_t kTileVec = 2u;   // source and destination allow 16-byte vectors
+
+constexpr int kRsThreads = 256;
+constexpr int kAgThreads = 256;
+
+// Arguments of the reduce-scatter kernel.  gtab is param-major
+// (gtab[p * N + k] = rank k's gradient of p) so one tile's N pointers are
+// contiguous; stab is rank-major (stab[r * P + p]).
+struct RsArgs {
+  const Tile* tiles;
+  int64_t num_tiles;
+  const uint16_t* const* gtab;
+  float* const* stab;
+  int32_t num_ranks;
+  int32_t num_params;
+  float scale;
+};
+
+struct AgArgs {
+  const Tile* tiles;
+  int64_t num_tiles;
+  const uint16_t* buf;
+  uint16_t* const* ptab;
+};
+
+// Kernel launchers (kernels.cu).  Return the launch's cudaError_t.
+cudaError_t launch_rs(const RsArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_ag(const AgArgs& a, int grid, cudaStream_t stream);
+// Resident CTAs per SM of each kernel for `num_ranks` (RS) at its block size.
+cudaError_t rs_occupancy(int32_t num_ranks, int* blocks_per_sm);
+cudaError_t ag_occupancy(int* blocks_per_sm);
+size_t rs_smem_bytes(int32_t num_ranks);
+
+// Device-side pointer table, cached by content.
+struct PtrSlot {
+  std::vector<uintptr_t> key;   // op tag followed by the host pointer table(s)
+  void** d_table = nullptr;     // device copy
+  void** h_staging = nullptr;   // pinned staging for the upload
+  size_t capacity = 0;          // entries
+  cudaEvent_t upload_ev = nullptr;
+  cudaEvent_t use_ev = nullptr;
+  cudaStream_t upload_stream = nullptr;
+  bool used = false;
+  uint64_t last_use = 0;
+};
+constexpr int kPtrSlots = 8;
+
+}  // namespace tide
+
+struct tide_layout_s {
+  int32_t num_ranks = 0;
+  int32_t num_params = 0;
+  int64_t align = 8;
+  std::vector<int64_t> d0, inner, chunk, shard_numel, offset;
+  int64_t block_numel = 0;  // S
+  std::vector<tide::Tile> rs_tiles, ag_tiles;
+  tide_mode_t mode = TIDE_MODE_UNCAPPED;
+  int32_t cta_cap = 0;
+
+  // device state, created on first compute call
+  int device = -1;
+  tide::Tile* d_rs_tiles = nullptr;
+  tide::Tile* d_ag_tiles = nullptr;
+  int num_sms = 0;
+  int rs_occ = 0, ag_occ = 0;
+  int max_pitch = 0;
+  tide::PtrSlot slots[tide::kPtrSlots];
+  uint64_t use_counter = 0;
+  std::mutex mu;
+};
+
+namespace tide {
+tide_status_t set_error(tide_status_t st, const std::string& msg);
+tide_status_t cuda_fail(cudaError_t e, const char* what);
+int rs_grid(const tide_layout_s* l);
+int ag_grid(const tide_layout_s* l);
+}  // namespace tide

@@ -1,0 +1,236 @@
+"""ctypes binding of libtide.so (declared in include/tide.h).
+
+Argument marshalling only: every step of the reduce-scatter and placement
+runs in the library's CUDA kernels (or, for copy-engine placement, in CUDA
+copies the library enqueues).  There is no Python or CPU fallback: if the
+library is missing, importing this module raises.
+
+Pointer arguments accept ints (raw device addresses), objects with a
+``data_ptr()`` method (e.g. torch tensors), or a prebuilt ``PointerTable``.
+Streams accept ints (cudaStream_t values), objects with a ``cuda_stream``
+attribute (e.g. torch.cuda.Stream), or None for the legacy default stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtide.so")
+
+TIDE_OK = 0
+TIDE_ERR_INVALID_ARG = 1
+TIDE_ERR_MISALIGNED = 2
+TIDE_ERR_UNSUPPORTED = 3
+TIDE_ERR_CUDA = 4
+TIDE_ERR_TIMEOUT = 5
+TIDE_ERR_OUT_OF_MEMORY = 6
+
+TIDE_MODE_UNCAPPED = 0
+TIDE_MODE_CAPPED = 1
+TIDE_MODE_COPY_ENGINE = 2
+
+TIDE_OP_RS = 0
+TIDE_OP_AG = 1
+
+TIDE_MAX_RANKS = 4096
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python __graft_entry__.py` "
+                      "(the CUDA library is required; there is no fallback)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_vp = ctypes.c_void_p
+_st = ctypes.c_int
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+
+
+def _sig(name, res, *args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = list(args)
+    return f
+
+
+_sig("tide_layout_create", _st, ctypes.c_int32, _vp, _vp, ctypes.c_int32, ctypes.POINTER(_vp))
+_sig("tide_layout_create_ex", _st, ctypes.c_int32, _vp, _vp, ctypes.c_int32, ctypes.c_int64,
+     ctypes.POINTER(_vp))
+_sig("tide_layout_destroy", None, _vp)
+_sig("tide_layout_num_params", _st, _vp, _i32p)
+_sig("tide_layout_num_ranks", _st, _vp, _i32p)
+_sig("tide_layout_rank_block_numel", _st, _vp, _i64p)
+_sig("tide_layout_shard_numel", _st, _vp, ctypes.c_int32, _i64p)
+_sig("tide_layout_param_offset", _st, _vp, ctypes.c_int32, _i64p)
+_sig("tide_layout_valid_rows", _st, _vp, ctypes.c_int32, ctypes.c_int32, _i64p)
+_sig("tide_layout_chunk_rows", _st, _vp, ctypes.c_int32, _i64p)
+_sig("tide_layout_set_mode", _st, _vp, ctypes.c_int, ctypes.c_int32)
+_sig("tide_layout_launch_shape", _st, _vp, ctypes.c_int, _i32p, _i32p)
+_sig("tide_layout_tiles", _st, _vp, ctypes.c_int, _vp, ctypes.c_int64, _i64p)
+_sig("tide_rs_bf16_to_fp32", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
+_sig("tide_ag_place", _st, _vp, _vp, _vp, _vp)
+_sig("tide_status_string", ctypes.c_char_p, _st)
+_sig("tide_last_error", ctypes.c_char_p)
+
+
+class TideError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.tide_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {tide_status_string(status)}" + (f" — {msg}" if msg else ""))
+
+
+def _check(status: int, where: str) -> None:
+    if status != TIDE_OK:
+        raise TideError(status, where)
+
+
+def _addr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s) -> int:
+    if s is None:
+        return 0
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+class PointerTable:
+    """A host array of device pointers, built once and reused across calls."""
+
+    def __init__(self, items):
+        addrs = [_addr(x) for x in items]
+        self.n = len(addrs)
+        self.array = (ctypes.c_void_p * max(1, self.n))(*addrs)
+        self.keep = list(items)  # keep tensors alive while the table exists
+
+    @property
+    def ptr(self) -> int:
+        return ctypes.addressof(self.array)
+
+
+def _table(x) -> int:
+    if x is None:
+        return 0
+    if not isinstance(x, PointerTable):
+        x = PointerTable(x)
+    return x.ptr if x.n else 0
+
+
+def tide_status_string(status: int) -> str:
+    return _lib.tide_status_string(status).decode()
+
+
+def tide_last_error() -> str:
+    return _lib.tide_last_error().decode(errors="replace")
+
+
+def _shape_arrays(shapes):
+    nd = np.asarray([len(s) for s in shapes], dtype=np.int32)
+    flat = np.asarray([int(d) for s in shapes for d in s], dtype=np.int64)
+    return nd, flat
+
+
+def tide_layout_create(shapes, num_ranks: int, align_elems: int | None = None) -> int:
+    """Layout handle for parameters of the given shapes over num_ranks ranks."""
+    nd, flat = _shape_arrays(shapes)
+    out = ctypes.c_void_p(0)
+    nd_p = nd.ctypes.data if nd.size else 0
+    fl_p = flat.ctypes.data if flat.size else 0
+    if align_elems is None:
+        st = _lib.tide_layout_create(len(shapes), nd_p, fl_p, num_ranks, ctypes.byref(out))
+    else:
+        st = _lib.tide_layout_create_ex(len(shapes), nd_p, fl_p, num_ranks, align_elems,
+                                        ctypes.byref(out))
+    _check(st, "tide_layout_create")
+    return out.value
+
+
+def tide_layout_destroy(layout: int) -> None:
+    _lib.tide_layout_destroy(layout)
+
+
+def _q64(fn, *args):
+    v = ctypes.c_int64(0)
+    _check(getattr(_lib, fn)(*args, ctypes.byref(v)), fn)
+    return v.value
+
+
+def _q32(fn, *args):
+    v = ctypes.c_int32(0)
+    _check(getattr(_lib, fn)(*args, ctypes.byref(v)), fn)
+    return v.value
+
+
+def tide_layout_num_params(layout) -> int:
+    return _q32("tide_layout_num_params", layout)
+
+
+def tide_layout_num_ranks(layout) -> int:
+    return _q32("tide_layout_num_ranks", layout)
+
+
+def tide_layout_rank_block_numel(layout) -> int:
+    return _q64("tide_layout_rank_block_numel", layout)
+
+
+def tide_layout_shard_numel(layout, p: int) -> int:
+    return _q64("tide_layout_shard_numel", layout, p)
+
+
+def tide_layout_param_offset(layout, p: int) -> int:
+    return _q64("tide_layout_param_offset", layout, p)
+
+
+def tide_layout_valid_rows(layout, p: int, r: int) -> int:
+    return _q64("tide_layout_valid_rows", layout, p, r)
+
+
+def tide_layout_chunk_rows(layout, p: int) -> int:
+    return _q64("tide_layout_chunk_rows", layout, p)
+
+
+def tide_layout_set_mode(layout, mode: int, cta_cap: int = 0) -> None:
+    _check(_lib.tide_layout_set_mode(layout, mode, cta_cap), "tide_layout_set_mode")
+
+
+def tide_layout_launch_shape(layout, op: int):
+    g, b = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(_lib.tide_layout_launch_shape(layout, op, ctypes.byref(g), ctypes.byref(b)),
+           "tide_layout_launch_shape")
+    return g.value, b.value
+
+
+def tide_layout_tiles(layout, op: int) -> np.ndarray:
+    """(count, 6) int64 array: param, rank, src_offset, dst_offset, length, flags."""
+    n = ctypes.c_int64(0)
+    _check(_lib.tide_layout_tiles(layout, op, 0, 0, ctypes.byref(n)), "tide_layout_tiles")
+    rows = np.zeros((max(1, n.value), 6), dtype=np.int64)
+    _check(_lib.tide_layout_tiles(layout, op, rows.ctypes.data, n.value, ctypes.byref(n)),
+           "tide_layout_tiles")
+    return rows[: n.value]
+
+
+def tide_rs_bf16_to_fp32(layout, grads, shards, scale: float, stream=None) -> None:
+    """grads: N*P rank-major bf16 gradient pointers; shards: N*P fp32 shard pointers."""
+    _check(_lib.tide_rs_bf16_to_fp32(layout, _table(grads), _table(shards), scale,
+                                     _stream(stream)), "tide_rs_bf16_to_fp32")
+
+
+def tide_ag_place(layout, gathered, params, stream=None) -> None:
+    """gathered: N*S bf16 rank-major buffer; params: P bf16 parameter pointers."""
+    _check(_lib.tide_ag_place(layout, _addr(gathered), _table(params), _stream(stream)),
+           "tide_ag_place")
+
+
+def exported_symbols():
+    """Names of the ABI functions this binding resolved (for load checks)."""
+    return [n for n in dir(_lib) if n.startswith("tide_")]

@@ -1,0 +1,189 @@
+"""CUDA path (through the C ABI) against the CPU oracle.
+
+Small jobs are compared element by element over every output; full-size
+workloads on sampled outputs the oracle computes one by one, plus a PyTorch
+fp32 reference over every element.  Reduce-scatter is summed in rank order
+on both sides, so every comparison is bit-exact.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import gpu_checks  # noqa: E402
+import synth  # noqa: E402
+from synth.device import DeviceJob  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU-only hosts
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import layout_aware_collectives_gb300 as tide  # noqa: E402
+
+MODES = [("uncapped", tide.TIDE_MODE_UNCAPPED, 0)] + [
+    (f"capped{c}", tide.TIDE_MODE_CAPPED, c) for c in (1, 2, 7, 8, 32)]
+
+
+def run(job, rs_mode=None, ag_mode=None, scale=None):
+    lay = job.layout
+    if rs_mode is not None:
+        lay.set_mode(*rs_mode)
+    lay.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), job.wl.scale if scale is None else scale)
+    if ag_mode is not None:
+        lay.set_mode(*ag_mode)
+    lay.place(job.gathered, job.param_ptrs())
+    torch.cuda.synchronize()
+
+
+@pytest.fixture
+def tiny_job():
+    wl = synth.tiny()
+    lay = tide.Layout(wl.shapes, wl.num_ranks)
+    job = DeviceJob(wl, lay)
+    yield job
+    lay.close()
+
+
+def test_device_generator_matches_host(tiny_job):
+    job = tiny_job
+    for k in range(job.N):
+        for p in range(job.P):
+            got = job.grads[k][p].cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, job.wl.host_grad(k, p)), (k, p)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=[m[0] for m in MODES])
+def test_tiny_full_parity(tiny_job, mode):
+    job = tiny_job
+    gpu_checks.check_layout(job)
+    run(job, rs_mode=mode[1:], ag_mode=mode[1:])
+    gpu_checks.full_check_rs(job)
+    gpu_checks.full_check_ag(job)
+    assert job.guards_intact()
+
+
+def test_tiny_copy_engine_placement(tiny_job):
+    job = tiny_job
+    job.layout.set_mode(tide.TIDE_MODE_COPY_ENGINE)
+    job.layout.place(job.gathered, job.param_ptrs())
+    torch.cuda.synchronize()
+    gpu_checks.full_check_ag(job)
+    assert job.guards_intact()
+    with pytest.raises(tide.TideError) as e:
+        job.layout.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), 0.25)
+    assert e.value.status == tide.TIDE_ERR_UNSUPPORTED
+
+
+def test_repeated_calls_and_pointer_cache(tiny_job):
+    """Same buffers (cache hit), fresh outputs (miss) and more distinct
+    pointer sets than cache slots (eviction) all give the oracle's result."""
+    job = tiny_job
+    for _ in range(3):
+        job.reset_outputs()
+        run(job)
+        gpu_checks.full_check_rs(job)
+    wl = job.wl
+    jobs = [DeviceJob(wl, job.layout, fill=False) for _ in range(10)]
+    for j in jobs:
+        j.grads = job.grads
+        j.gathered = job.gathered
+        run(j)
+    for j in jobs[::3]:
+        gpu_checks.full_check_rs(j)
+        gpu_checks.full_check_ag(j)
+
+
+def test_other_stream(tiny_job):
+    job = tiny_job
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    job.layout.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), job.wl.scale, stream=s)
+    job.layout.place(job.gathered, job.param_ptrs(), stream=s)
+    s.synchronize()
+    gpu_checks.full_check_rs(job)
+    gpu_checks.full_check_ag(job)
+
+
+def _ragged_cases():
+    rng = np.random.default_rng(11)
+    cases = []
+    for n in (1, 2, 3, 5, 8, 13, 16, 64):
+        shapes = [(int(rng.integers(1, 3 * n + 5)), int(rng.integers(1, 40)))
+                  for _ in range(4)]
+        shapes += [(n - 1 if n > 1 else 1, 24), (3 * n + 1,), (), (0, 16), (7, 0, 3),
+                   (2 * n, 3, 5)]
+        cases.append((n, shapes))
+    return cases
+
+
+@pytest.mark.parametrize("align", [8, 1])
+@pytest.mark.parametrize("case", _ragged_cases(), ids=lambda c: f"N{c[0]}")
+def test_ragged_shapes_full_parity(case, align):
+    """d0 < N (empty ranks), d0 not a multiple of N, inner not a multiple of
+    8, 0-dim scalars, zero-size tensors, 3-D tensors, unaligned offsets."""
+    n, shapes = case
+    wl = synth.custom(f"ragged{n}", n, shapes, sigma=0.5, seed=n)
+    with tide.Layout(wl.shapes, n, align_elems=align) as lay:
+        job = DeviceJob(wl, lay, align=align)
+        gpu_checks.check_layout(job)
+        for mode in MODES[:3]:
+            job.reset_outputs()
+            run(job, rs_mode=mode[1:], ag_mode=mode[1:], scale=0.3)
+            gpu_checks.full_check_rs(job, scale=0.3)
+            gpu_checks.full_check_ag(job)
+            assert job.guards_intact()
+
+
+def test_empty_layout():
+    with tide.Layout([], 4) as lay:
+        lay.reduce_scatter([], [], 0.25)
+        lay.place(None, [])
+        torch.cuda.synchronize()
+    with tide.Layout([(0, 8)], 4) as lay:
+        lay.reduce_scatter([None] * 4, [None] * 4, 0.25)
+        lay.place(None, [None])
+        torch.cuda.synchronize()
+
+
+FULL = ["llama8b", "llama70b", "moe", "sweep16", "sweep32", "sweep64"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_parity(name):
+    """Full-size workloads in the bench's launch configuration (uncapped):
+    sampled elements of every (rank, param) against the oracle, every element
+    against a PyTorch fp32 reference; capped mode on the same inputs agrees
+    bit for bit."""
+    wl = synth.WORKLOADS[name]()
+    with tide.Layout(wl.shapes, wl.num_ranks) as lay:
+        job = DeviceJob(wl, lay, guard=False)
+        gpu_checks.check_layout(job)
+        run(job)
+        assert gpu_checks.sampled_check_rs(job) > 0
+        assert gpu_checks.sampled_check_ag(job) > 0
+        gpu_checks.torch_check_rs(job)
+        gpu_checks.torch_check_ag(job)
+        ref = [s.clone() for s in (job.shards[0][0], job.shards[-1][-1])]
+        lay.set_mode(tide.TIDE_MODE_CAPPED, 64)
+        for row in job.shards:
+            for s in row:
+                s.fill_(float("nan"))
+        run(job)
+        assert torch.equal(job.shards[0][0], ref[0]) and torch.equal(job.shards[-1][-1], ref[1])
+        gpu_checks.torch_check_rs(job)
+        del job
+        torch.cuda.empty_cache()
+
+
+def test_int64_offsets():
+    """A parameter of more than 2^31 elements: offsets past 32-bit range."""
+    d0 = (1 << 31) // 4096 + 17
+    wl = synth.custom("huge", 2, [(d0, 4096), (5,)], sigma=1e-3, seed=3)
+    with tide.Layout(wl.shapes, 2) as lay:
+        job = DeviceJob(wl, lay, guard=False)
+        run(job)
+        assert gpu_checks.sampled_check_rs(job, per=32) > 0
+        assert gpu_checks.sampled_check_ag(job, per=64) > 0
+        del job
+        torch.cuda.empty_cache()

@@ -117,12 +117,16 @@ class PointerTable:
         return ctypes.addressof(self.array)
 
 
-def _table(x) -> int:
+def _table(x) -> PointerTable | None:
+    """A PointerTable for x; the caller keeps it referenced across the C call
+    so the host array outlives the library's read of it."""
     if x is None:
-        return 0
-    if not isinstance(x, PointerTable):
-        x = PointerTable(x)
-    return x.ptr if x.n else 0
+        return None
+    return x if isinstance(x, PointerTable) else PointerTable(x)
+
+
+def _tptr(t: PointerTable | None) -> int:
+    return t.ptr if t is not None and t.n else 0
 
 
 def tide_status_string(status: int) -> str:
@@ -221,14 +225,15 @@ def tide_layout_tiles(layout, op: int) -> np.ndarray:
 
 def tide_rs_bf16_to_fp32(layout, grads, shards, scale: float, stream=None) -> None:
     """grads: N*P rank-major bf16 gradient pointers; shards: N*P fp32 shard pointers."""
-    _check(_lib.tide_rs_bf16_to_fp32(layout, _table(grads), _table(shards), scale,
-                                     _stream(stream)), "tide_rs_bf16_to_fp32")
+    g, s = _table(grads), _table(shards)
+    _check(_lib.tide_rs_bf16_to_fp32(layout, _tptr(g), _tptr(s), scale, _stream(stream)),
+           "tide_rs_bf16_to_fp32")
 
 
 def tide_ag_place(layout, gathered, params, stream=None) -> None:
     """gathered: N*S bf16 rank-major buffer; params: P bf16 parameter pointers."""
-    _check(_lib.tide_ag_place(layout, _addr(gathered), _table(params), _stream(stream)),
-           "tide_ag_place")
+    t = _table(params)
+    _check(_lib.tide_ag_place(layout, _addr(gathered), _tptr(t), _stream(stream)), "tide_ag_place")
 
 
 def exported_symbols():

@@ -31,11 +31,13 @@ int grid_for(int64_t n) {
 
 }  // namespace
 
+#define SYNTH_EXPORT __attribute__((visibility("default")))
+
 extern "C" {
 
 // out[i] = synth_bf16(key, first + i, ...) for i in [0, n), on `stream`.
 // Returns the cudaError_t of the launch (0 on success).
-int synth_fill_bf16_device(uint16_t* out, int64_t n, uint64_t key, uint64_t first, float amp,
+SYNTH_EXPORT int synth_fill_bf16_device(uint16_t* out, int64_t n, uint64_t key, uint64_t first, float amp,
                            uint32_t outlier_every, float outlier_mult, void* stream) {
   if (n <= 0) return 0;
   synth_fill_kernel<<<grid_for(n), 256, 0, (cudaStream_t)stream>>>(out, n, key, first, amp,
@@ -44,7 +46,7 @@ int synth_fill_bf16_device(uint16_t* out, int64_t n, uint64_t key, uint64_t firs
 }
 
 // out[i] = v for i in [0, n): sentinel and guard-band fills.
-int synth_set_u16_device(uint16_t* out, int64_t n, uint16_t v, void* stream) {
+SYNTH_EXPORT int synth_set_u16_device(uint16_t* out, int64_t n, uint16_t v, void* stream) {
   if (n <= 0) return 0;
   synth_set_u16_kernel<<<grid_for(n), 256, 0, (cudaStream_t)stream>>>(out, n, v);
   return (int)cudaGetLastError();

@@ -71,3 +71,10 @@ def test_host_fill_matches_gather():
     full = w.host_grad(2, 7)
     idx = np.array([0, 17, 249])
     assert np.array_equal(w.host_grad_at(2, 7, idx), full[idx])
+
+
+def test_device_generator_library_exports():
+    import ctypes
+
+    lib = ctypes.CDLL(synth.DEVICE_LIB)
+    assert hasattr(lib, "synth_fill_bf16_device") and hasattr(lib, "synth_set_u16_device")

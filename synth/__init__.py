@@ -217,6 +217,15 @@ def llama70b() -> Workload:
                         outlier_every=100, outlier_mult=100.0)
 
 
+def llama70b_attn() -> Workload:
+    """The attention projections of the 70B-shaped layer alone (q,o [8192,8192],
+    k,v [1024,8192], N=8, same outliers): a 3.6 GB case of the same kernel
+    shape for profiler captures."""
+    w = llama70b()
+    return Workload("llama70b_attn", 8, w.shapes[:4], w.names[:4], w.sigma,
+                    outlier_every=w.outlier_every, outlier_mult=w.outlier_mult)
+
+
 def moe() -> Workload:
     """Qwen3-30B-A3B-shaped MoE layer, N=16, 128 experts, ~30% unrouted per rank."""
     shapes = [(4096, 2048), (512, 2048), (512, 2048), (2048, 4096), (128, 2048)]
@@ -259,6 +268,7 @@ WORKLOADS = {
     "llama8b": llama8b,
     "llama70b": llama70b,
     "moe": moe,
+    "llama70b_attn": llama70b_attn,
     "sweep16": lambda: sweep(16),
     "sweep32": lambda: sweep(32),
     "sweep64": lambda: sweep(64),

@@ -199,6 +199,40 @@ TIDE_API tide_status_t tide_rs_bf16_to_fp32(tide_layout_t layout, const uint16_t
 TIDE_API tide_status_t tide_ag_place(tide_layout_t layout, const uint16_t* gathered,
                             uint16_t* const* params, cudaStream_t stream);
 
+/* Bytes of the device array behind tide_rs_bf16_to_fp32_noalloc. */
+#define TIDE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * Reduce-scatter that allocates nothing.  The pages have no counterpart: it
+ * exists for callers that cannot call cudaMalloc — for example a framework
+ * whose caching allocator owns all device memory and must not see
+ * allocations it does not track, a process under a hard device-memory cap
+ * with every byte reserved, or a step that cannot absorb the device-wide
+ * synchronisation of a later cudaFree.  tide_rs_bf16_to_fp32 allocates its
+ * device tile list and pointer tables on a layout's first call; this variant
+ * never does, so together with the host-only tide_layout_create a caller can
+ * run the reduce-scatter without any allocation.
+ *
+ * Same arguments, result (bit for bit) and modes as tide_rs_bf16_to_fp32.
+ * The kernel's scratch (the layout's tile list, 32 bytes per tile, plus
+ * 2*N*P device pointers) is copied on `stream` into one file-scope device
+ * array of TIDE_NOALLOC_SCRATCH_BYTES (4 MiB) that every GPU loading the
+ * library holds until the process exits; a layout that needs more returns
+ * TIDE_ERR_INVALID_ARG without enqueuing anything.  Every byte the kernel
+ * reads from the array is written by the same call, so nothing has to start
+ * at zero.  All calls share the array, which keeps the last call's tables:
+ * calls that overlap on the GPU (on different streams, or from different
+ * layouts without stream ordering between them) race.  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress);
+ * make that first call before any stream capture.  The tables are copied
+ * from pageable host memory, so the call returns once the driver has taken
+ * its copy of them.  No cudaMalloc, cudaFree or other allocating routine is
+ * called.
+ */
+TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t layout, const uint16_t* const* grads,
+                                                    float* const* shards, float scale,
+                                                    cudaStream_t stream);
+
 /* Static description of a status code. */
 TIDE_API const char* tide_status_string(tide_status_t status);
 

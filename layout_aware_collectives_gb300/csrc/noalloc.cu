@@ -1,0 +1,130 @@
+// Reduce-scatter entry point that allocates no memory.
+//
+// The regular tide_rs_bf16_to_fp32 keeps its tile list and pointer tables in
+// device memory it allocates (cudaMalloc, plus pinned staging from
+// cudaMallocHost) on a layout's first call.  Some callers cannot allow that:
+// a framework whose caching allocator owns all device memory and must not
+// see allocations it does not track, a process running under a hard
+// device-memory cap with every byte already reserved, or a step that cannot
+// absorb the device-wide synchronisation a later cudaFree implies.  Layouts
+// are built on the host without any CUDA call, so with this entry point such
+// a caller runs the whole reduce-scatter without a single allocation.
+//
+// The kernel's scratch (tile list + gradient and shard pointer tables) lives
+// in one file-scope __device__ array of kNoallocScratchBytes that every GPU
+// loading this library holds until the process exits.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "tide_internal.h"
+
+namespace tide {
+namespace {
+
+constexpr size_t kNoallocScratchBytes = TIDE_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device.  In host
+// code the symbol name is only a host-side stand-in, never a device address.
+std::mutex g_setup_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+tide_status_t scratch_for_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return set_error(TIDE_ERR_UNSUPPORTED, "device ordinal beyond the no-allocation table");
+  std::lock_guard<std::mutex> g(g_setup_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return TIDE_OK;
+}
+
+tide_status_t check(const void* p, int64_t numel, const char* what, int64_t i) {
+  if (numel == 0) return TIDE_OK;
+  if (!p) return set_error(TIDE_ERR_INVALID_ARG, std::string(what) + "[" + std::to_string(i) + "] is NULL");
+  if ((uintptr_t)p & 15u)
+    return set_error(TIDE_ERR_MISALIGNED,
+                     std::string(what) + "[" + std::to_string(i) + "] is not 16-byte aligned");
+  return TIDE_OK;
+}
+
+}  // namespace
+}  // namespace tide
+
+using namespace tide;
+
+extern "C" TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t l,
+                                                               const uint16_t* const* grads,
+                                                               float* const* shards, float scale,
+                                                               cudaStream_t stream) {
+  if (!l) return set_error(TIDE_ERR_INVALID_ARG, "layout is NULL");
+  const int32_t N = l->num_ranks, P = l->num_params;
+  if (P > 0 && (!grads || !shards)) return set_error(TIDE_ERR_INVALID_ARG, "pointer table is NULL");
+  std::lock_guard<std::mutex> g(l->mu);
+  if (l->mode == TIDE_MODE_COPY_ENGINE)
+    return set_error(TIDE_ERR_UNSUPPORTED, "reduce-scatter has no copy-engine mode");
+  for (int64_t i = 0; i < (int64_t)N * P; ++i) {
+    tide_status_t st = check(grads[i], l->d0[i % P] * l->inner[i % P], "grads", i);
+    if (st == TIDE_OK) st = check(shards[i], l->shard_numel[i % P], "shards", i);
+    if (st != TIDE_OK) return st;
+  }
+  if (l->rs_tiles.empty()) return TIDE_OK;
+
+  const size_t tile_bytes = sizeof(Tile) * l->rs_tiles.size();
+  const size_t table_bytes = sizeof(void*) * 2 * (size_t)N * P;
+  if (tile_bytes + table_bytes > kNoallocScratchBytes)
+    return set_error(TIDE_ERR_INVALID_ARG,
+                     "layout needs " + std::to_string(tile_bytes + table_bytes) +
+                         " bytes of scratch (tile list + pointer tables); the no-allocation "
+                         "entry point holds at most " + std::to_string(kNoallocScratchBytes));
+  void* scratch = nullptr;
+  tide_status_t st = scratch_for_current_device(&scratch);
+  if (st != TIDE_OK) return st;
+
+  int dev = 0, sms = 0, occ = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = rs_occupancy(N, &occ);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  const int64_t tiles = (int64_t)l->rs_tiles.size();
+  const int64_t want = l->mode == TIDE_MODE_CAPPED ? (int64_t)l->cta_cap : (int64_t)sms * std::max(1, occ);
+  const int grid = (int)std::min<int64_t>(tiles, want);
+
+  // Scratch layout: [tile list][param-major gradient table][rank-major shard table].
+  std::vector<const void*> table(2 * (size_t)N * P);
+  for (int32_t p = 0; p < P; ++p)
+    for (int32_t k = 0; k < N; ++k) table[(size_t)p * N + k] = grads[(size_t)k * P + p];
+  for (int64_t i = 0; i < (int64_t)N * P; ++i) table[(size_t)N * P + i] = shards[i];
+  unsigned char* base = (unsigned char*)scratch;
+  // Pageable sources: each copy returns once the driver holds its own copy of
+  // the bytes, so the host vectors may go out of scope after the calls.
+  e = cudaMemcpyAsync(base, l->rs_tiles.data(), tile_bytes, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(base + tile_bytes, table.data(), table_bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "copy of the tables into the no-allocation scratch");
+
+  RsArgs a;
+  a.tiles = (const Tile*)base;
+  a.num_tiles = tiles;
+  a.gtab = (const uint16_t* const*)(base + tile_bytes);
+  a.stab = (float* const*)(base + tile_bytes) + (size_t)N * P;
+  a.num_ranks = N;
+  a.num_params = P;
+  a.scale = scale;
+  e = launch_rs(a, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter kernel launch");
+  return TIDE_OK;
+}

@@ -36,6 +36,7 @@ TIDE_OP_RS = 0
 TIDE_OP_AG = 1
 
 TIDE_MAX_RANKS = 4096
+TIDE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with `python __graft_entry__.py` "
@@ -71,6 +72,7 @@ _sig("tide_layout_launch_shape", _st, _vp, ctypes.c_int, _i32p, _i32p)
 _sig("tide_layout_tiles", _st, _vp, ctypes.c_int, _vp, ctypes.c_int64, _i64p)
 _sig("tide_rs_bf16_to_fp32", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
 _sig("tide_ag_place", _st, _vp, _vp, _vp, _vp)
+_sig("tide_rs_bf16_to_fp32_noalloc", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
 _sig("tide_status_string", ctypes.c_char_p, _st)
 _sig("tide_last_error", ctypes.c_char_p)
 
@@ -228,6 +230,14 @@ def tide_rs_bf16_to_fp32(layout, grads, shards, scale: float, stream=None) -> No
     g, s = _table(grads), _table(shards)
     _check(_lib.tide_rs_bf16_to_fp32(layout, _tptr(g), _tptr(s), scale, _stream(stream)),
            "tide_rs_bf16_to_fp32")
+
+
+def tide_rs_bf16_to_fp32_noalloc(layout, grads, shards, scale: float, stream=None) -> None:
+    """As tide_rs_bf16_to_fp32, for callers that cannot allocate device memory:
+    the kernel's tables go into the library's fixed 4 MiB device array."""
+    g, s = _table(grads), _table(shards)
+    _check(_lib.tide_rs_bf16_to_fp32_noalloc(layout, _tptr(g), _tptr(s), scale, _stream(stream)),
+           "tide_rs_bf16_to_fp32_noalloc")
 
 
 def tide_ag_place(layout, gathered, params, stream=None) -> None:

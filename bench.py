@@ -73,14 +73,23 @@ def barrier(world):
 
 
 def reduce_max(x: float, world: int) -> float:
+    """Maximum of x over all ranks (the slowest replica's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(step_ms_local: float, bytes_per_step: int, world: int):
+    """Whole-job figures of N independent replicas: every rank moves
+    bytes_per_step per step; the job's step time is the slowest rank's."""
+    step_ms = reduce_max(step_ms_local, world)
+    return step_ms, world * bytes_per_step / (step_ms * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------- clocks
@@ -363,8 +372,7 @@ def run_tide(args):
         step_ms_local = ev[0][0].elapsed_time(ev[K - 1][2]) / K
     else:
         step_ms_local = sum(r + a for r, a in zip(rs_ms, ag_ms)) / K
-    step_ms = reduce_max(step_ms_local, world)
-    value = world * (rs_bytes + ag_bytes) / (step_ms * 1e-3) / 1e9
+    step_ms, value = aggregate(step_ms_local, rs_bytes + ag_bytes, world)
     rs_avg = statistics.mean(rs_ms)
     ag_avg = statistics.mean(ag_ms)
 
@@ -460,8 +468,7 @@ def run_e2e(tide, layout, job, wl, stream, K, world):
         e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    ms = reduce_max(e0.elapsed_time(e1) / steps, world)
-    val = world * (wl.rs_bytes() + wl.ag_bytes()) / (ms * 1e-3) / 1e9
+    ms, val = aggregate(e0.elapsed_time(e1) / steps, wl.rs_bytes() + wl.ag_bytes(), world)
     del h_g, h_s, h_buf, h_p
     return {"value": round(val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": steps}

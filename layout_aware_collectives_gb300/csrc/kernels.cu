@@ -95,11 +95,15 @@ __device__ __forceinline__ void rs_group(float (&acc)[V][8], const uint16_t* con
 // groups of G ranks (all G*V 16-byte loads before any add) and the adds run
 // in ascending rank order, so the fp32 result equals the sequential sum
 // acc = ((0 + g_0) + g_1) + ... + g_{N-1}, then one multiply by the scale.
-// NFIX > 0 fixes N at compile time (full unroll, no predicates).
-template <int NFIX, int G, int V>
-__global__ void __launch_bounds__(kRsThreads) rs_kernel(RsArgs a) {
-  extern __shared__ const uint16_t* s_src[];  // the current tile's N source pointers
+// NFIX > 0 fixes N at compile time (full unroll, no predicates).  The N
+// source pointers of a tile are staged in shared memory, double-buffered so
+// one barrier per tile suffices: a thread can only write buffer b again after
+// every thread has passed the barrier of the tile in between.
+template <int THREADS, int NFIX, int G, int V>
+__global__ void __launch_bounds__(THREADS, TIDE_RS_MIN_BLOCKS) rs_kernel(RsArgs a) {
+  extern __shared__ const uint16_t* s_src[];  // [2][N] source pointers
   const int N = NFIX > 0 ? NFIX : a.num_ranks;
+  int buf = 0;
   for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
     float* __restrict__ out = a.stab[(int64_t)tile.r * a.num_params + tile.p] + tile.dst;
@@ -107,36 +111,40 @@ __global__ void __launch_bounds__(kRsThreads) rs_kernel(RsArgs a) {
     if (tile.flags & kTileZero) {  // padding rows of the shard
       if (tile.flags & kTileVec) {
         const int nv = tile.len >> 2;
-        for (int i = threadIdx.x; i < nv; i += blockDim.x) st_stream(out + 4 * i, 0.f, 0.f, 0.f, 0.f);
-        for (int e = 4 * nv + threadIdx.x; e < tile.len; e += blockDim.x) out[e] = 0.f;
+        for (int i = threadIdx.x; i < nv; i += THREADS) st_stream(out + 4 * i, 0.f, 0.f, 0.f, 0.f);
+        for (int e = 4 * nv + threadIdx.x; e < tile.len; e += THREADS) out[e] = 0.f;
       } else {
-        for (int e = threadIdx.x; e < tile.len; e += blockDim.x) out[e] = 0.f;
+        for (int e = threadIdx.x; e < tile.len; e += THREADS) out[e] = 0.f;
       }
       continue;
     }
 
-    __syncthreads();  // every thread is done with the previous tile's pointers
-    for (int k = threadIdx.x; k < N; k += blockDim.x)
-      s_src[k] = a.gtab[(int64_t)tile.p * N + k] + tile.src;
+    const uint16_t** sp = s_src + buf * N;
+    buf ^= 1;
+    for (int k = threadIdx.x; k < N; k += THREADS) sp[k] = a.gtab[(int64_t)tile.p * N + k] + tile.src;
     __syncthreads();
 
     if (tile.flags & kTileVec) {
       const int nvec = tile.len >> 3;
-      for (int v0 = threadIdx.x; v0 < nvec; v0 += V * blockDim.x) {
+      for (int v0 = threadIdx.x; v0 < nvec; v0 += V * THREADS) {
         float acc[V][8];
 #pragma unroll
         for (int u = 0; u < V; ++u)
 #pragma unroll
           for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
-        if constexpr (NFIX > 0) {
+        if constexpr (NFIX > 0 && (THREADS <= 256 || NFIX <= G)) {
 #pragma unroll
-          for (int k0 = 0; k0 < NFIX; k0 += G) rs_group<G, V, true>(acc, s_src, k0, N, v0, nvec);
+          for (int k0 = 0; k0 < NFIX; k0 += G) rs_group<G, V, true>(acc, sp, k0, N, v0, nvec);
+        } else if constexpr (NFIX > 0) {
+          // fat CTAs: one group of loads in flight per thread, no spills
+#pragma unroll 1
+          for (int k0 = 0; k0 < NFIX; k0 += G) rs_group<G, V, true>(acc, sp, k0, N, v0, nvec);
         } else {
-          for (int k0 = 0; k0 < N; k0 += G) rs_group<G, V, false>(acc, s_src, k0, N, v0, nvec);
+          for (int k0 = 0; k0 < N; k0 += G) rs_group<G, V, false>(acc, sp, k0, N, v0, nvec);
         }
 #pragma unroll
         for (int u = 0; u < V; ++u) {
-          const int v = v0 + u * blockDim.x;
+          const int v = v0 + u * THREADS;
           if (v < nvec) {
             float* o = out + 8 * v;
             st_stream(o, __fmul_rn(acc[u][0], a.scale), __fmul_rn(acc[u][1], a.scale),
@@ -146,15 +154,15 @@ __global__ void __launch_bounds__(kRsThreads) rs_kernel(RsArgs a) {
           }
         }
       }
-      for (int e = 8 * nvec + threadIdx.x; e < tile.len; e += blockDim.x) {
+      for (int e = 8 * nvec + threadIdx.x; e < tile.len; e += THREADS) {
         float acc = 0.f;
-        for (int k = 0; k < N; ++k) acc = __fadd_rn(acc, bf16_f32(ld_stream_u16(s_src[k] + e)));
+        for (int k = 0; k < N; ++k) acc = __fadd_rn(acc, bf16_f32(ld_stream_u16(sp[k] + e)));
         out[e] = __fmul_rn(acc, a.scale);
       }
     } else {  // a run whose source is not 16-byte aligned: element by element
-      for (int e = threadIdx.x; e < tile.len; e += blockDim.x) {
+      for (int e = threadIdx.x; e < tile.len; e += THREADS) {
         float acc = 0.f;
-        for (int k = 0; k < N; ++k) acc = __fadd_rn(acc, bf16_f32(ld_stream_u16(s_src[k] + e)));
+        for (int k = 0; k < N; ++k) acc = __fadd_rn(acc, bf16_f32(ld_stream_u16(sp[k] + e)));
         out[e] = __fmul_rn(acc, a.scale);
       }
     }
@@ -165,75 +173,86 @@ __global__ void __launch_bounds__(kRsThreads) rs_kernel(RsArgs a) {
 // One tile = a contiguous run of rank r's chunk of parameter p: a copy from
 // gathered[r*S + o_p + ...] to params[p][r*c_p*inner_p + ...].  U 16-byte
 // vectors per thread are loaded before any is stored.
-template <int U>
-__global__ void __launch_bounds__(kAgThreads) ag_kernel(AgArgs a) {
+template <int THREADS, int U>
+__global__ void __launch_bounds__(THREADS) ag_kernel(AgArgs a) {
   for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
     const uint16_t* __restrict__ src = a.buf + tile.src;
     uint16_t* __restrict__ dst = a.ptab[tile.p] + tile.dst;
     if (tile.flags & kTileVec) {
       const int nvec = tile.len >> 3;
-      for (int v0 = threadIdx.x; v0 < nvec; v0 += U * blockDim.x) {
+      for (int v0 = threadIdx.x; v0 < nvec; v0 += U * THREADS) {
         uint4 d[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (v0 + u * (int)blockDim.x < nvec) d[u] = ld_stream(src + 8 * (v0 + u * blockDim.x));
+          if (v0 + u * THREADS < nvec) d[u] = ld_stream(src + 8 * (v0 + u * THREADS));
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (v0 + u * (int)blockDim.x < nvec) st_stream(dst + 8 * (v0 + u * blockDim.x), d[u]);
+          if (v0 + u * THREADS < nvec) st_stream(dst + 8 * (v0 + u * THREADS), d[u]);
       }
-      for (int e = 8 * nvec + threadIdx.x; e < tile.len; e += blockDim.x) dst[e] = ld_stream_u16(src + e);
+      for (int e = 8 * nvec + threadIdx.x; e < tile.len; e += THREADS) dst[e] = ld_stream_u16(src + e);
     } else {
-      for (int e = threadIdx.x; e < tile.len; e += blockDim.x) dst[e] = ld_stream_u16(src + e);
+      for (int e = threadIdx.x; e < tile.len; e += THREADS) dst[e] = ld_stream_u16(src + e);
     }
   }
 }
 
-constexpr int kAgUnroll = 4;
-
 // ---------------------------------------------------------------- dispatch
 using RsKernel = void (*)(RsArgs);
+using AgKernel = void (*)(AgArgs);
 
+template <int T>
 RsKernel rs_kernel_for(int32_t n) {
   switch (n) {
-    case 1: return rs_kernel<1, 1, 8>;
-    case 2: return rs_kernel<2, 2, 4>;
-    case 3: return rs_kernel<3, 3, 2>;
-    case 4: return rs_kernel<4, 4, 2>;
-    case 5: return rs_kernel<5, 5, 1>;
-    case 6: return rs_kernel<6, 6, 1>;
-    case 7: return rs_kernel<7, 7, 1>;
-    case 8: return rs_kernel<8, 8, 1>;
-    case 16: return rs_kernel<16, 8, 1>;
-    case 32: return rs_kernel<32, 8, 1>;
-    case 64: return rs_kernel<64, 8, 1>;
-    default: return rs_kernel<0, 8, 1>;
+    case 1: return rs_kernel<T, 1, 1, 8>;
+    case 2: return rs_kernel<T, 2, 2, 4>;
+    case 3: return rs_kernel<T, 3, 3, 2>;
+    case 4: return rs_kernel<T, 4, 4, 2>;
+    case 5: return rs_kernel<T, 5, 5, 1>;
+    case 6: return rs_kernel<T, 6, 6, 1>;
+    case 7: return rs_kernel<T, 7, 7, 1>;
+    case 8: return rs_kernel<T, 8, 8, 1>;
+    case 16: return rs_kernel<T, 16, 8, 1>;
+    case 32: return rs_kernel<T, 32, 8, 1>;
+    case 64: return rs_kernel<T, 64, 8, 1>;
+    default: return rs_kernel<T, 0, 8, 1>;
   }
+}
+
+RsKernel rs_kernel_for(int32_t n, bool fat) {
+  return fat ? rs_kernel_for<kFatThreads>(n) : rs_kernel_for<kRsThreads>(n);
+}
+
+AgKernel ag_kernel_for(bool fat) {
+  return fat ? ag_kernel<kFatThreads, TIDE_AG_UNROLL> : ag_kernel<kAgThreads, TIDE_AG_UNROLL>;
 }
 
 }  // namespace
 
-size_t rs_smem_bytes(int32_t num_ranks) { return sizeof(const uint16_t*) * (size_t)num_ranks; }
+size_t rs_smem_bytes(int32_t num_ranks) { return 2 * sizeof(const uint16_t*) * (size_t)num_ranks; }
 
-cudaError_t launch_rs(const RsArgs& a, int grid, cudaStream_t stream) {
+int rs_block(bool fat) { return fat ? kFatThreads : kRsThreads; }
+int ag_block(bool fat) { return fat ? kFatThreads : kAgThreads; }
+
+cudaError_t launch_rs(const RsArgs& a, int grid, bool fat, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
-  rs_kernel_for(a.num_ranks)<<<grid, kRsThreads, rs_smem_bytes(a.num_ranks), stream>>>(a);
+  rs_kernel_for(a.num_ranks, fat)<<<grid, rs_block(fat), rs_smem_bytes(a.num_ranks), stream>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_ag(const AgArgs& a, int grid, cudaStream_t stream) {
+cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
-  ag_kernel<kAgUnroll><<<grid, kAgThreads, 0, stream>>>(a);
+  ag_kernel_for(fat)<<<grid, ag_block(fat), 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t rs_occupancy(int32_t num_ranks, int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, rs_kernel_for(num_ranks),
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, rs_kernel_for(num_ranks, false),
                                                        kRsThreads, rs_smem_bytes(num_ranks));
 }
 
 cudaError_t ag_occupancy(int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, ag_kernel<kAgUnroll>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, ag_kernel_for(false),
                                                        kAgThreads, 0);
 }
 

@@ -24,14 +24,15 @@ bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow
 
 int64_t roundup(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-// Elements per reduce-scatter tile: about 256 KiB of bf16 reads across the N
-// ranks, at least one full CTA pass (256 threads x 8 elements).
+// Elements per reduce-scatter tile: TIDE_RS_TILE_READ_BYTES (256 KiB) of
+// bf16 reads across the N ranks, at least one full CTA pass (8 elements per
+// thread).
 int64_t rs_tile_elems(int32_t n) {
-  int64_t t = (int64_t)131072 / n;
-  t = std::max<int64_t>(2048, std::min<int64_t>(65536, t));
+  int64_t t = (int64_t)TIDE_RS_TILE_READ_BYTES / 2 / n;
+  t = std::max<int64_t>(8 * TIDE_RS_THREADS, std::min<int64_t>(65536, t));
   return t / 8 * 8;
 }
-constexpr int64_t kAgTileElems = 32768;    // 64 KiB read + 64 KiB written
+constexpr int64_t kAgTileElems = TIDE_AG_TILE_ELEMS;  // 64 KiB read + 64 KiB written
 constexpr int64_t kZeroTileElems = 65536;  // padding fill
 
 // Split [0, n) into near-equal runs of at most `t` elements, each run but

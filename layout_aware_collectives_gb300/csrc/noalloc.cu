@@ -124,7 +124,7 @@ extern "C" TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t l,
   a.num_ranks = N;
   a.num_params = P;
   a.scale = scale;
-  e = launch_rs(a, grid, stream);
+  e = launch_rs(a, grid, l->mode == TIDE_MODE_CAPPED, stream);
   if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter kernel launch");
   return TIDE_OK;
 }

@@ -229,12 +229,12 @@ tide_status_t tide_layout_launch_shape(tide_layout_t l, tide_op_t op, int32_t* g
     *grid = l->mode == TIDE_MODE_COPY_ENGINE
                 ? 0
                 : grid_for((int64_t)l->rs_tiles.size(), l->mode, l->cta_cap, d.sms, d.rs_occ);
-    *block = kRsThreads;
+    *block = rs_block(l->mode == TIDE_MODE_CAPPED);
   } else {
     *grid = l->mode == TIDE_MODE_COPY_ENGINE
                 ? 0
                 : grid_for((int64_t)l->ag_tiles.size(), l->mode, l->cta_cap, d.sms, d.ag_occ);
-    *block = kAgThreads;
+    *block = ag_block(l->mode == TIDE_MODE_CAPPED);
   }
   return TIDE_OK;
 }
@@ -277,7 +277,7 @@ tide_status_t tide_rs_bf16_to_fp32(tide_layout_t l, const uint16_t* const* grads
   a.num_ranks = N;
   a.num_params = P;
   a.scale = scale;
-  cudaError_t e = launch_rs(a, rs_grid(l), stream);
+  cudaError_t e = launch_rs(a, rs_grid(l), l->mode == TIDE_MODE_CAPPED, stream);
   if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter kernel launch");
   return mark_used(l, slot, stream);
 }
@@ -316,7 +316,7 @@ tide_status_t tide_ag_place(tide_layout_t l, const uint16_t* gathered, uint16_t*
   a.num_tiles = (int64_t)l->ag_tiles.size();
   a.buf = gathered;
   a.ptab = (uint16_t* const*)slot->d_table;
-  cudaError_t e = launch_ag(a, ag_grid(l), stream);
+  cudaError_t e = launch_ag(a, ag_grid(l), l->mode == TIDE_MODE_CAPPED, stream);
   if (e != cudaSuccess) return cuda_fail(e, "placement kernel launch");
   return mark_used(l, slot, stream);
 }

@@ -29,8 +29,32 @@ static_assert(sizeof(Tile) == 32, "Tile is 32 bytes");
 constexpr uint32_t kTileZero = 1u;  // RS only: write +0.0f (padding rows)
 constexpr uint32_t kTileVec = 2u;   // source and destination allow 16-byte vectors
 
-constexpr int kRsThreads = 256;
-constexpr int kAgThreads = 256;
+// Launch and tiling constants.  Each can be overridden at build time with the
+// macro of the same name (used to sweep launch shapes).
+#ifndef TIDE_RS_THREADS
+#define TIDE_RS_THREADS 256
+#endif
+#ifndef TIDE_AG_THREADS
+#define TIDE_AG_THREADS 256
+#endif
+#ifndef TIDE_AG_UNROLL
+#define TIDE_AG_UNROLL 4
+#endif
+#ifndef TIDE_RS_TILE_READ_BYTES  // bf16 bytes read per RS tile across all N ranks
+#define TIDE_RS_TILE_READ_BYTES 262144
+#endif
+#ifndef TIDE_AG_TILE_ELEMS
+#define TIDE_AG_TILE_ELEMS 32768
+#endif
+#ifndef TIDE_FAT_THREADS  // block of the CTA-capped mode: one fat CTA per occupied SM
+#define TIDE_FAT_THREADS 1024
+#endif
+#ifndef TIDE_RS_MIN_BLOCKS  // __launch_bounds__ min blocks per SM of the RS kernel
+#define TIDE_RS_MIN_BLOCKS 1
+#endif
+constexpr int kRsThreads = TIDE_RS_THREADS;
+constexpr int kAgThreads = TIDE_AG_THREADS;
+constexpr int kFatThreads = TIDE_FAT_THREADS;
 
 // Arguments of the reduce-scatter kernel.  gtab is param-major
 // (gtab[p * N + k] = rank k's gradient of p) so one tile's N pointers are
@@ -52,9 +76,14 @@ struct AgArgs {
   uint16_t* const* ptab;
 };
 
-// Kernel launchers (kernels.cu).  Return the launch's cudaError_t.
-cudaError_t launch_rs(const RsArgs& a, int grid, cudaStream_t stream);
-cudaError_t launch_ag(const AgArgs& a, int grid, cudaStream_t stream);
+// Kernel launchers (kernels.cu).  Return the launch's cudaError_t.  `fat`
+// selects the kFatThreads-wide CTA used by the CTA-capped mode: a capped CTA
+// takes its SM away from full-SM compute kernels anyway, so it brings as many
+// loads in flight as one SM holds.
+cudaError_t launch_rs(const RsArgs& a, int grid, bool fat, cudaStream_t stream);
+cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, cudaStream_t stream);
+int rs_block(bool fat);
+int ag_block(bool fat);
 // Resident CTAs per SM of each kernel for `num_ranks` (RS) at its block size.
 cudaError_t rs_occupancy(int32_t num_ranks, int* blocks_per_sm);
 cudaError_t ag_occupancy(int* blocks_per_sm);

@@ -45,6 +45,16 @@ def lib():
         L.oracle_ag_source_index.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_int64]
+        L.oracle_rs_rank.restype = None
+        L.oracle_rs_rank.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_float, ctypes.c_int32]
+        L.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+        L.oracle_ag_pack.restype = None
+        L.oracle_ag_pack.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                     ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
         _lib = L
     return _lib
 
@@ -133,3 +143,40 @@ def ag_source_index(num_ranks, shape, offset, block_numel, i, j) -> int:
     d0, inner = _dims([shape])
     return lib().oracle_ag_source_index(num_ranks, int(d0[0]), int(inner[0]), offset,
                                         block_numel, i, j)
+
+
+def rs_rank(shapes, num_ranks: int, grads, scale: float, r: int):
+    """Rank r's shards only: list of P fp32 arrays."""
+    P = len(shapes)
+    d0, inner = _dims(shapes)
+    g = [np.ascontiguousarray(grads[k][p], dtype=np.uint16)
+         for k in range(num_ranks) for p in range(P)]
+    out = [np.empty(chunk_rows(int(d0[p]), num_ranks) * int(inner[p]), dtype=np.float32)
+           for p in range(P)]
+    gp, op = _ptrs(g), _ptrs(out)
+    lib().oracle_rs_rank(num_ranks, P, d0.ctypes.data, inner.ctypes.data, gp.ctypes.data,
+                         op.ctypes.data, scale, r)
+    return out
+
+
+def f32_to_bf16(x) -> np.ndarray:
+    """Element-wise fp32 -> bf16 bits by the oracle's rounding."""
+    bits = np.ascontiguousarray(x, dtype=np.float32).ravel().view(np.uint32)
+    f = lib().oracle_f32_to_bf16
+    # pass the exact fp32 bits (a round trip through a Python float would
+    # quieten signalling NaNs before the oracle sees them)
+    return np.array([f(ctypes.c_float.from_buffer_copy(int(b).to_bytes(4, "little")))
+                     for b in bits], dtype=np.uint16)
+
+
+def ag_pack(shapes, num_ranks: int, offsets, block_numel: int, r: int, shards_r, gathered):
+    """Writes rank r's block of `gathered` (uint16 array, modified in place)."""
+    P = len(shapes)
+    d0, inner = _dims(shapes)
+    src = [np.ascontiguousarray(shards_r[p], dtype=np.float32) for p in range(P)]
+    offs = np.ascontiguousarray(offsets, dtype=np.int64)
+    assert gathered.dtype == np.uint16 and gathered.flags.c_contiguous
+    sp = _ptrs(src)
+    lib().oracle_ag_pack(num_ranks, P, d0.ctypes.data, inner.ctypes.data, offs.ctypes.data,
+                         block_numel, r, sp.ctypes.data, gathered.ctypes.data)
+    return gathered

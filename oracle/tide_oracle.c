@@ -100,3 +100,45 @@ void oracle_ag_place(int32_t num_ranks, int32_t num_params, const int64_t* d0,
             gathered[oracle_ag_source_index(num_ranks, d0[p], inner[p], offsets[p], block_numel,
                                             i, j)];
 }
+
+void oracle_rs_rank(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                    const uint16_t* const* grads, float* const* shards_r, float scale, int32_t r) {
+  uint16_t vals[4096];
+  for (int32_t p = 0; p < num_params; ++p) {
+    const int64_t c = oracle_chunk_rows(d0[p], num_ranks);
+    for (int64_t ii = 0; ii < c; ++ii) {
+      const int64_t i = (int64_t)r * c + ii;
+      for (int64_t j = 0; j < inner[p]; ++j) {
+        if (i < d0[p]) {
+          for (int32_t k = 0; k < num_ranks; ++k)
+            vals[k] = grads[(int64_t)k * num_params + p][i * inner[p] + j];
+          shards_r[p][ii * inner[p] + j] = oracle_rs_element(num_ranks, vals, scale);
+        } else {
+          shards_r[p][ii * inner[p] + j] = 0.0f;
+        }
+      }
+    }
+  }
+}
+
+/* Round to nearest even on the 16 bits dropped: add half an ulp of bf16
+ * (0x7FFF) plus the lowest kept bit, then truncate. */
+uint16_t oracle_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x0040u); /* NaN */
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* FSDP2 all-gather input: the rank's padded shard in the parameter dtype,
+ * at its place in the rank-major buffer ([TIDE] "FSDP2通信开销的根源"). */
+void oracle_ag_pack(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                    const int64_t* offsets, int64_t block_numel, int32_t r,
+                    const float* const* shards_r, uint16_t* gathered) {
+  for (int32_t p = 0; p < num_params; ++p) {
+    const int64_t n = oracle_chunk_rows(d0[p], num_ranks) * inner[p];
+    for (int64_t e = 0; e < n; ++e)
+      gathered[(int64_t)r * block_numel + offsets[p] + e] = oracle_f32_to_bf16(shards_r[p][e]);
+  }
+}

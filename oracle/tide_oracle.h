@@ -78,6 +78,23 @@ void oracle_ag_place(int32_t num_ranks, int32_t num_params, const int64_t* d0,
 int64_t oracle_ag_source_index(int32_t num_ranks, int64_t d0, int64_t inner, int64_t offset,
                                int64_t block_numel, int64_t i, int64_t j);
 
+/* Reduce-scatter output of one rank only: shards_r[p] (c_p * inner[p] fp32)
+ * receives exactly what oracle_rs writes to shards[r * P + p]. */
+void oracle_rs_rank(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                    const uint16_t* const* grads, float* const* shards_r, float scale, int32_t r);
+
+/* fp32 -> bf16 bits, round to nearest, ties to even; NaN keeps its sign and
+ * top payload bits and becomes quiet; overflow rounds to infinity. */
+uint16_t oracle_f32_to_bf16(float f);
+
+/* All-gather input pack of rank r (FSDP2's cast of the fp32 shard to the
+ * bf16 parameter dtype, written into the rank's block of the rank-major
+ * buffer): gathered[r * S + o_p + e] = bf16(shards_r[p][e]) for every
+ * e < c_p * inner[p], padding rows included.  Alignment gaps are untouched. */
+void oracle_ag_pack(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                    const int64_t* offsets, int64_t block_numel, int32_t r,
+                    const float* const* shards_r, uint16_t* gathered);
+
 #ifdef __cplusplus
 }
 #endif

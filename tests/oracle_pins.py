@@ -337,3 +337,66 @@ ALL_CHECKS = [
     check_rs_f64_bound, check_rs_special_values, check_ag_golden, check_ag_identity,
     check_rs_ag_composition,
 ]
+
+
+# ---------------------------------------------------------------- single-rank RS and AG input pack
+def check_bf16_rounding_golden():
+    for row in load_golden("bf16_rounding.txt"):
+        f = np.array([int(row[0], 16)], dtype=np.uint32).view(np.float32)
+        got = int(oracle.f32_to_bf16(f)[0])
+        assert got == int(row[1], 16), (row[0], hex(got), row[1])
+
+
+def check_bf16_rounding_vs_torch(seed=8):
+    """Finite values against torch's own fp32 -> bfloat16 conversion."""
+    rng = np.random.default_rng(seed)
+    bits = rng.integers(0, 2**32, size=20000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    x = np.concatenate([x, (rng.standard_normal(5000) * 1e-3).astype(np.float32)])
+    assert np.array_equal(oracle.f32_to_bf16(x), f32_to_bf16_rne(x))
+
+
+def check_rs_rank_matches_full(seed=9):
+    rng = np.random.default_rng(seed)
+    for n in (1, 3, 4, 8):
+        shapes = [(2 * n + 1, 3), (n - 1 if n > 1 else 1,), (5, 2, 2)]
+        grads = [[random_bf16(rng, dims(s)[0] * dims(s)[1]) for s in shapes] for _ in range(n)]
+        full = oracle.rs(shapes, n, grads, 0.5)
+        for r in range(n):
+            one = oracle.rs_rank(shapes, n, grads, 0.5, r)
+            for p in range(len(shapes)):
+                assert np.array_equal(fp32_bits(one[p]), fp32_bits(full[r][p])), (n, r, p)
+
+
+def check_pack_then_place(seed=10):
+    """Every rank packs its fp32 shards; placement of the result gives the
+    bf16 (torch rounding) of the full reduced tensor; padding slots of each
+    shard carry bf16 +0 and alignment gaps keep the sentinel."""
+    rng = np.random.default_rng(seed)
+    for n in (2, 3, 4):
+        shapes = [(7, 5), (11,), (3, 4)]
+        grads = [[random_bf16(rng, dims(s)[0] * dims(s)[1]) for s in shapes] for _ in range(n)]
+        shards = oracle.rs(shapes, n, grads, 1.0 / n)
+        offs, S = oracle.layout(shapes, n, 8)
+        buf = np.full(n * S, SENTINEL, dtype=np.uint16)
+        for r in range(n):
+            oracle.ag_pack(shapes, n, offs, S, r, shards[r], buf)
+        placed = oracle.ag_place(shapes, n, buf, offs, S)
+        want = brute_force_rs(shapes, n, grads, 1.0 / n)
+        written = np.zeros(n * S, dtype=bool)
+        for p, s in enumerate(shapes):
+            d0, inner = dims(s)
+            full = np.concatenate([want[r][p] for r in range(n)])[: d0 * inner]
+            assert np.array_equal(placed[p], f32_to_bf16_rne(full)), (n, p)
+            c = oracle.chunk_rows(d0, n)
+            for r in range(n):
+                v = oracle.valid_rows(d0, n, r) * inner
+                blk = buf[r * S + offs[p]: r * S + offs[p] + c * inner]
+                assert np.all(blk[v:] == 0)  # padding rows: bf16(+0.0)
+                written[r * S + offs[p]: r * S + offs[p] + c * inner] = True
+        assert np.all(buf[~written] == SENTINEL)
+
+
+ALL_CHECKS += [check_bf16_rounding_golden, check_bf16_rounding_vs_torch, check_rs_rank_matches_full,
+               check_pack_then_place]

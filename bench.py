@@ -406,6 +406,7 @@ def run_tide(args):
         "device": props.name,
     }
 
+    out["next_ops"] = run_next_ops(tide, layout, job, wl, stream)
     if not args.no_e2e:
         out["e2e"] = run_e2e(tide, layout, job, wl, stream, K, world)
     if not args.no_interference:
@@ -421,6 +422,43 @@ def run_tide(args):
 
         dist.destroy_process_group()
     return 0
+
+
+def run_next_ops(tide, layout, job, wl, stream, reps=20):
+    """Device time of the per-GPU operations next to the step: the
+    single-rank reduce-scatter (rank 0: what one GPU of the job computes) and
+    the all-gather input pack of every rank (fp32 shard -> bf16 slot)."""
+    import torch
+
+    N = wl.num_ranks
+    valid0 = sum(max(0, min(c, d0 - 0 * c)) * inner
+                 for c, (d0, inner) in zip(job.chunk, job.dims))
+    padded = sum(job.shard_numel)
+    outs = [torch.empty(n, dtype=torch.float32, device="cuda") for n in job.shard_numel]
+    job.make_pack_inputs()
+    gptr = tide.PointerTable(job.grad_ptrs())
+    optr = tide.PointerTable(outs)
+    pptr = tide.PointerTable(job.pack_src_ptrs())
+    res = {}
+    for name, op, nbytes in (
+            ("rs_rank0", lambda: layout.reduce_scatter_rank(0, gptr, optr, wl.scale, stream),
+             2 * N * valid0 + 4 * valid0),
+            ("ag_pack_all_ranks", lambda: layout.pack(-1, pptr, job.packed, stream),
+             6 * N * padded)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                op()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                op()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"ms": round(ms, 4), "bytes": nbytes,
+                     "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    del outs, job.pack_src, job.packed
+    return res
 
 
 def run_e2e(tide, layout, job, wl, stream, K, world):

@@ -95,7 +95,9 @@ typedef enum {
   TIDE_MODE_COPY_ENGINE = 2
 } tide_mode_t;
 
-typedef enum { TIDE_OP_RS = 0, TIDE_OP_AG = 1 } tide_op_t;
+/* Operations, for the launch-shape and tile-list queries: the
+ * reduce-scatter, the placement and the all-gather input pack. */
+typedef enum { TIDE_OP_RS = 0, TIDE_OP_AG = 1, TIDE_OP_PACK = 2 } tide_op_t;
 
 /* Maximum simulated ranks per layout. */
 #define TIDE_MAX_RANKS 4096
@@ -198,6 +200,42 @@ TIDE_API tide_status_t tide_rs_bf16_to_fp32(tide_layout_t layout, const uint16_t
  */
 TIDE_API tide_status_t tide_ag_place(tide_layout_t layout, const uint16_t* gathered,
                             uint16_t* const* params, cudaStream_t stream);
+
+/*
+ * Reduce-scatter output of ONE rank: what a single GPU of an FSDP2 job keeps
+ * after the collective ("FSDP2通信开销的根源": each rank ends with one
+ * reduced shard).  Same arithmetic as tide_rs_bf16_to_fp32, restricted to
+ * rank `rank`:
+ *   shards[p][i'*inner_p + j] = scale * sum_k f32(grads[k*P + p][(rank*c_p + i')*inner_p + j])
+ * (+0.0f in padding rows), summed in ascending k from +0.0f.
+ *   rank    0 .. N-1;
+ *   grads   host array of N*P device pointers, as for tide_rs_bf16_to_fp32;
+ *   shards  host array of P device pointers: that rank's fp32 shard of each
+ *           parameter (c_p*inner_p elements, 16-byte aligned).
+ * Reads N*(c_p rows) of every gradient instead of all rows.  Modes as for
+ * tide_rs_bf16_to_fp32 (TIDE_ERR_UNSUPPORTED in TIDE_MODE_COPY_ENGINE).
+ */
+TIDE_API tide_status_t tide_rs_bf16_to_fp32_rank(tide_layout_t layout, int32_t rank,
+                                                 const uint16_t* const* grads, float* const* shards,
+                                                 float scale, cudaStream_t stream);
+
+/*
+ * All-gather input pack: FSDP2 gathers each rank's padded shard in the bf16
+ * parameter dtype, so after the optimizer step a rank casts its fp32 shard
+ * to bf16 into its slot of the rank-major buffer ("FSDP2通信开销的根源"):
+ *   gathered[r*S + o_p + e] = bf16_rne(shards_r[p][e])   for e < c_p*inner_p,
+ * padding rows included; bf16_rne rounds to nearest, ties to even, keeps
+ * NaN (quiet, sign and top payload kept) and rounds overflow to infinity.
+ * Alignment gaps between shards are not written.
+ *   rank      0 .. N-1: `shards` holds P device pointers (that rank's fp32
+ *             shards) and only block `rank` is written;
+ *             -1: `shards` holds N*P pointers (rank-major, as the output of
+ *             tide_rs_bf16_to_fp32) and every block is written;
+ *   gathered  device pointer to the N*S bf16 buffer (16-byte aligned).
+ * TIDE_ERR_UNSUPPORTED in TIDE_MODE_COPY_ENGINE (a cast needs the SMs).
+ */
+TIDE_API tide_status_t tide_ag_pack_bf16(tide_layout_t layout, int32_t rank, const float* const* shards,
+                                         uint16_t* gathered, cudaStream_t stream);
 
 /* Bytes of the device array behind tide_rs_bf16_to_fp32_noalloc. */
 #define TIDE_NOALLOC_SCRATCH_BYTES (4u << 20)

@@ -197,6 +197,50 @@ __global__ void __launch_bounds__(THREADS) ag_kernel(AgArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- all-gather input pack
+// fp32 -> bf16 bits, round to nearest with ties to even on the 16 dropped
+// bits (the usual add-half-ulp-plus-lowest-kept-bit method); a NaN keeps its
+// sign and top payload and is made quiet.
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (u >> 16) | 0x0040u;
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+}
+
+// One tile = a run of rank r's fp32 shard of parameter p, cast to bf16 into
+// its slot gathered[r*S + o_p + ...].  Per 8 elements: two 16-byte loads,
+// one 16-byte store.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) pack_kernel(PackArgs a) {
+  for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+    const Tile tile = a.tiles[t];
+    const float* __restrict__ src = a.stab[(int64_t)tile.r * a.num_params + tile.p] + tile.src;
+    uint16_t* __restrict__ dst = a.buf + tile.dst;
+    int e0 = 0;
+    if (tile.flags & kTileVec) {
+      const int nvec = tile.len >> 3;
+      for (int v = threadIdx.x; v < nvec; v += THREADS) {
+        const uint4 x = ld_stream(src + 8 * v);
+        const uint4 y = ld_stream(src + 8 * v + 4);
+        uint4 o;
+        o.x = pack2(__uint_as_float(x.x), __uint_as_float(x.y));
+        o.y = pack2(__uint_as_float(x.z), __uint_as_float(x.w));
+        o.z = pack2(__uint_as_float(y.x), __uint_as_float(y.y));
+        o.w = pack2(__uint_as_float(y.z), __uint_as_float(y.w));
+        st_stream(dst + 8 * v, o);
+      }
+      e0 = 8 * nvec;
+    }
+    for (int e = e0 + threadIdx.x; e < tile.len; e += THREADS)
+      dst[e] = (uint16_t)f32_to_bf16_bits(src[e]);
+  }
+}
+
 // ---------------------------------------------------------------- dispatch
 using RsKernel = void (*)(RsArgs);
 using AgKernel = void (*)(AgArgs);
@@ -244,6 +288,22 @@ cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, cudaStream_t stream) 
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
   ag_kernel_for(fat)<<<grid, ag_block(fat), 0, stream>>>(a);
   return cudaGetLastError();
+}
+
+int pk_block(bool fat) { return fat ? kFatThreads : kAgThreads; }
+
+cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, cudaStream_t stream) {
+  if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
+  if (fat)
+    pack_kernel<kFatThreads><<<grid, kFatThreads, 0, stream>>>(a);
+  else
+    pack_kernel<kAgThreads><<<grid, kAgThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t pk_occupancy(int* blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pack_kernel<kAgThreads>,
+                                                       kAgThreads, 0);
 }
 
 cudaError_t rs_occupancy(int32_t num_ranks, int* blocks_per_sm) {

@@ -50,9 +50,14 @@ void build_tiles(tide_layout_s* l) {
   const int64_t T = rs_tile_elems(N);
   l->rs_tiles.clear();
   l->ag_tiles.clear();
-  for (int32_t p = 0; p < l->num_params; ++p) {
-    const int64_t c = l->chunk[p], inner = l->inner[p], d0 = l->d0[p];
-    for (int32_t r = 0; r < N; ++r) {
+  l->pk_tiles.clear();
+  l->rs_rank_begin.assign(1, 0);
+  l->pk_rank_begin.assign(1, 0);
+  // rank-major: one rank's tiles are contiguous (single-rank calls launch a
+  // sub-range of the list)
+  for (int32_t r = 0; r < N; ++r) {
+    for (int32_t p = 0; p < l->num_params; ++p) {
+      const int64_t c = l->chunk[p], inner = l->inner[p], d0 = l->d0[p];
       const int64_t v = std::max<int64_t>(0, std::min<int64_t>(c, d0 - (int64_t)r * c));
       const int64_t seg = v * inner;
       const int64_t rs_src = (int64_t)r * c * inner;
@@ -72,7 +77,15 @@ void build_tiles(tide_layout_s* l) {
         if (t.src % 8 == 0 && t.dst % 8 == 0) t.flags |= kTileVec;
         l->ag_tiles.push_back(t);
       });
+      // pack: the whole padded shard (padding rows are part of the AG input)
+      split_runs(c * inner, kAgTileElems, [&](int64_t s, int64_t n) {
+        Tile t{s, ag_src + s, (int32_t)n, p, r, 0u};
+        if (t.src % 4 == 0 && t.dst % 8 == 0) t.flags |= kTileVec;
+        l->pk_tiles.push_back(t);
+      });
     }
+    l->rs_rank_begin.push_back((int64_t)l->rs_tiles.size());
+    l->pk_rank_begin.push_back((int64_t)l->pk_tiles.size());
   }
 }
 
@@ -243,8 +256,10 @@ tide_status_t tide_layout_set_mode(tide_layout_t l, tide_mode_t mode, int32_t ct
 tide_status_t tide_layout_tiles(tide_layout_t l, tide_op_t op, int64_t* rows, int64_t cap,
                                 int64_t* count) {
   if (!l || !count) return set_error(TIDE_ERR_INVALID_ARG, "NULL argument");
-  if (op != TIDE_OP_RS && op != TIDE_OP_AG) return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
-  const std::vector<tide::Tile>& t = op == TIDE_OP_RS ? l->rs_tiles : l->ag_tiles;
+  if (op != TIDE_OP_RS && op != TIDE_OP_AG && op != TIDE_OP_PACK)
+    return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
+  const std::vector<tide::Tile>& t =
+      op == TIDE_OP_RS ? l->rs_tiles : op == TIDE_OP_AG ? l->ag_tiles : l->pk_tiles;
   *count = (int64_t)t.size();
   if (cap > 0 && !rows) return set_error(TIDE_ERR_INVALID_ARG, "rows is NULL");
   for (int64_t i = 0; i < std::min<int64_t>(cap, (int64_t)t.size()); ++i) {

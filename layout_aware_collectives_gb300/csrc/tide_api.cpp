@@ -18,7 +18,7 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
   } while (0)
 
 struct DeviceShape {
-  int sms = 0, rs_occ = 0, ag_occ = 0;
+  int sms = 0, rs_occ = 0, ag_occ = 0, pk_occ = 0;
 };
 
 tide_status_t query_device(const tide_layout_s* l, DeviceShape* d) {
@@ -28,8 +28,10 @@ tide_status_t query_device(const tide_layout_s* l, DeviceShape* d) {
             "cudaDeviceGetAttribute(MultiProcessorCount)");
   TIDE_CUDA(rs_occupancy(l->num_ranks, &d->rs_occ), "occupancy of the reduce-scatter kernel");
   TIDE_CUDA(ag_occupancy(&d->ag_occ), "occupancy of the placement kernel");
+  TIDE_CUDA(pk_occupancy(&d->pk_occ), "occupancy of the pack kernel");
   d->rs_occ = std::max(1, d->rs_occ);
   d->ag_occ = std::max(1, d->ag_occ);
+  d->pk_occ = std::max(1, d->pk_occ);
   return TIDE_OK;
 }
 
@@ -55,18 +57,21 @@ tide_status_t ensure_device(tide_layout_s* l) {
   if (st != TIDE_OK) return st;
   TIDE_CUDA(cudaDeviceGetAttribute(&l->max_pitch, cudaDevAttrMaxPitch, dev),
             "cudaDeviceGetAttribute(MaxPitch)");
-  const size_t rs_b = sizeof(Tile) * std::max<size_t>(1, l->rs_tiles.size());
-  const size_t ag_b = sizeof(Tile) * std::max<size_t>(1, l->ag_tiles.size());
-  TIDE_CUDA(cudaMalloc((void**)&l->d_rs_tiles, rs_b), "cudaMalloc(tile list)");
-  TIDE_CUDA(cudaMalloc((void**)&l->d_ag_tiles, ag_b), "cudaMalloc(tile list)");
-  if (!l->rs_tiles.empty())
-    TIDE_CUDA(cudaMemcpy(l->d_rs_tiles, l->rs_tiles.data(), sizeof(Tile) * l->rs_tiles.size(),
-                         cudaMemcpyHostToDevice),
-              "upload of the reduce-scatter tile list");
-  if (!l->ag_tiles.empty())
-    TIDE_CUDA(cudaMemcpy(l->d_ag_tiles, l->ag_tiles.data(), sizeof(Tile) * l->ag_tiles.size(),
-                         cudaMemcpyHostToDevice),
-              "upload of the placement tile list");
+  struct {
+    const std::vector<Tile>* host;
+    Tile** dev;
+    const char* what;
+  } lists[3] = {{&l->rs_tiles, &l->d_rs_tiles, "reduce-scatter tile list"},
+                {&l->ag_tiles, &l->d_ag_tiles, "placement tile list"},
+                {&l->pk_tiles, &l->d_pk_tiles, "pack tile list"}};
+  for (auto& t : lists) {
+    TIDE_CUDA(cudaMalloc((void**)t.dev, sizeof(Tile) * std::max<size_t>(1, t.host->size())),
+              "cudaMalloc(tile list)");
+    if (!t.host->empty())
+      TIDE_CUDA(cudaMemcpy(*t.dev, t.host->data(), sizeof(Tile) * t.host->size(),
+                           cudaMemcpyHostToDevice),
+                t.what);
+  }
   for (PtrSlot& s : l->slots) {
     TIDE_CUDA(cudaEventCreateWithFlags(&s.upload_ev, cudaEventDisableTiming), "cudaEventCreate");
     TIDE_CUDA(cudaEventCreateWithFlags(&s.use_ev, cudaEventDisableTiming), "cudaEventCreate");
@@ -74,6 +79,7 @@ tide_status_t ensure_device(tide_layout_s* l) {
   l->num_sms = d.sms;
   l->rs_occ = d.rs_occ;
   l->ag_occ = d.ag_occ;
+  l->pk_occ = d.pk_occ;
   l->device = dev;
   return TIDE_OK;
 }
@@ -184,17 +190,71 @@ tide_status_t ag_copy_engine(tide_layout_s* l, const uint16_t* buf, uint16_t* co
 
 }  // namespace
 
-int rs_grid(const tide_layout_s* l) {
-  return grid_for((int64_t)l->rs_tiles.size(), l->mode, l->cta_cap, l->num_sms, l->rs_occ);
-}
-
-int ag_grid(const tide_layout_s* l) {
-  return grid_for((int64_t)l->ag_tiles.size(), l->mode, l->cta_cap, l->num_sms, l->ag_occ);
+int grid_of(const tide_layout_s* l, int64_t tiles, int occ) {
+  return grid_for(tiles, l->mode, l->cta_cap, l->num_sms, occ);
 }
 
 }  // namespace tide
 
 using namespace tide;
+
+namespace tide {
+namespace {
+
+// Shared steps of the kernel entry points once arguments are validated: bind
+// the device, fetch the cached device pointer table, launch.
+tide_status_t run_rs(tide_layout_s* l, int64_t t0, int64_t t1, std::vector<uintptr_t>& key,
+                     const std::vector<void*>& entries, float scale, cudaStream_t stream) {
+  if (t1 <= t0) return TIDE_OK;
+  tide_status_t st = ensure_device(l);
+  if (st != TIDE_OK) return st;
+  PtrSlot* slot = nullptr;
+  st = acquire_table(l, key, entries, stream, &slot);
+  if (st != TIDE_OK) return st;
+  const int64_t NP = (int64_t)l->num_ranks * l->num_params;
+  RsArgs a;
+  a.tiles = l->d_rs_tiles + t0;
+  a.num_tiles = t1 - t0;
+  a.gtab = (const uint16_t* const*)slot->d_table;
+  a.stab = (float* const*)(slot->d_table + NP);
+  a.num_ranks = l->num_ranks;
+  a.num_params = l->num_params;
+  a.scale = scale;
+  cudaError_t e = launch_rs(a, grid_of(l, t1 - t0, l->rs_occ), l->mode == TIDE_MODE_CAPPED, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter kernel launch");
+  return mark_used(l, slot, stream);
+}
+
+// Gradient table (param-major) + shard table (rank-major) for the RS kernel;
+// shard entries of ranks not written stay null and are never read.
+tide_status_t rs_tables(tide_layout_s* l, int32_t rank, const uint16_t* const* grads,
+                        float* const* shards, std::vector<uintptr_t>* key,
+                        std::vector<void*>* entries) {
+  const int32_t N = l->num_ranks, P = l->num_params;
+  for (int64_t i = 0; i < (int64_t)N * P; ++i) {
+    tide_status_t st = check_ptr(grads[i], l->d0[i % P] * l->inner[i % P], "grads", i);
+    if (st != TIDE_OK) return st;
+  }
+  const int64_t nout = rank < 0 ? (int64_t)N * P : P;
+  for (int64_t i = 0; i < nout; ++i) {
+    tide_status_t st = check_ptr(shards[i], l->shard_numel[i % P], "shards", i);
+    if (st != TIDE_OK) return st;
+  }
+  entries->assign((size_t)2 * N * P, nullptr);
+  for (int32_t p = 0; p < P; ++p)
+    for (int32_t k = 0; k < N; ++k) (*entries)[(size_t)p * N + k] = (void*)grads[(size_t)k * P + p];
+  for (int64_t i = 0; i < nout; ++i)
+    (*entries)[(size_t)N * P + (rank < 0 ? i : (int64_t)rank * P + i)] = (void*)shards[i];
+  key->clear();
+  key->reserve(2 + entries->size());
+  key->push_back((uintptr_t)TIDE_OP_RS);
+  key->push_back((uintptr_t)(intptr_t)rank);
+  for (void* e : *entries) key->push_back((uintptr_t)e);
+  return TIDE_OK;
+}
+
+}  // namespace
+}  // namespace tide
 
 extern "C" {
 
@@ -213,6 +273,7 @@ void tide_layout_destroy(tide_layout_t l) {
     }
     cudaFree(l->d_rs_tiles);
     cudaFree(l->d_ag_tiles);
+    cudaFree(l->d_pk_tiles);
     if (cur >= 0 && cur != l->device) cudaSetDevice(cur);
   }
   delete l;
@@ -220,66 +281,51 @@ void tide_layout_destroy(tide_layout_t l) {
 
 tide_status_t tide_layout_launch_shape(tide_layout_t l, tide_op_t op, int32_t* grid, int32_t* block) {
   if (!l || !grid || !block) return set_error(TIDE_ERR_INVALID_ARG, "NULL argument");
-  if (op != TIDE_OP_RS && op != TIDE_OP_AG) return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
+  if (op != TIDE_OP_RS && op != TIDE_OP_AG && op != TIDE_OP_PACK)
+    return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
   std::lock_guard<std::mutex> g(l->mu);
   DeviceShape d;
   tide_status_t st = query_device(l, &d);
   if (st != TIDE_OK) return st;
-  if (op == TIDE_OP_RS) {
-    *grid = l->mode == TIDE_MODE_COPY_ENGINE
-                ? 0
-                : grid_for((int64_t)l->rs_tiles.size(), l->mode, l->cta_cap, d.sms, d.rs_occ);
-    *block = rs_block(l->mode == TIDE_MODE_CAPPED);
-  } else {
-    *grid = l->mode == TIDE_MODE_COPY_ENGINE
-                ? 0
-                : grid_for((int64_t)l->ag_tiles.size(), l->mode, l->cta_cap, d.sms, d.ag_occ);
-    *block = ag_block(l->mode == TIDE_MODE_CAPPED);
-  }
+  const bool capped = l->mode == TIDE_MODE_CAPPED;
+  const int64_t tiles = op == TIDE_OP_RS   ? (int64_t)l->rs_tiles.size()
+                        : op == TIDE_OP_AG ? (int64_t)l->ag_tiles.size()
+                                           : (int64_t)l->pk_tiles.size();
+  const int occ = op == TIDE_OP_RS ? d.rs_occ : op == TIDE_OP_AG ? d.ag_occ : d.pk_occ;
+  *grid = l->mode == TIDE_MODE_COPY_ENGINE ? 0 : grid_for(tiles, l->mode, l->cta_cap, d.sms, occ);
+  *block = op == TIDE_OP_RS ? rs_block(capped) : op == TIDE_OP_AG ? ag_block(capped) : pk_block(capped);
   return TIDE_OK;
 }
 
 tide_status_t tide_rs_bf16_to_fp32(tide_layout_t l, const uint16_t* const* grads, float* const* shards,
                                    float scale, cudaStream_t stream) {
   if (!l) return set_error(TIDE_ERR_INVALID_ARG, "layout is NULL");
-  const int32_t N = l->num_ranks, P = l->num_params;
-  if (P > 0 && (!grads || !shards)) return set_error(TIDE_ERR_INVALID_ARG, "pointer table is NULL");
+  if (l->num_params > 0 && (!grads || !shards))
+    return set_error(TIDE_ERR_INVALID_ARG, "pointer table is NULL");
   std::lock_guard<std::mutex> g(l->mu);
   if (l->mode == TIDE_MODE_COPY_ENGINE)
     return set_error(TIDE_ERR_UNSUPPORTED, "reduce-scatter has no copy-engine mode");
-  for (int64_t i = 0; i < (int64_t)N * P; ++i) {
-    tide_status_t st = check_ptr(grads[i], l->d0[i % P] * l->inner[i % P], "grads", i);
-    if (st == TIDE_OK) st = check_ptr(shards[i], l->shard_numel[i % P], "shards", i);
-    if (st != TIDE_OK) return st;
-  }
-  if (l->rs_tiles.empty()) return TIDE_OK;
-  tide_status_t st = ensure_device(l);
-  if (st != TIDE_OK) return st;
-
-  // device order: param-major gradient table, then rank-major shard table
   std::vector<uintptr_t> key;
-  key.reserve(1 + 2 * (size_t)N * P);
-  key.push_back((uintptr_t)TIDE_OP_RS);
-  std::vector<void*> entries((size_t)2 * N * P);
-  for (int32_t p = 0; p < P; ++p)
-    for (int32_t k = 0; k < N; ++k) entries[(size_t)p * N + k] = (void*)grads[(size_t)k * P + p];
-  for (int64_t i = 0; i < (int64_t)N * P; ++i) entries[(size_t)N * P + i] = (void*)shards[i];
-  for (void* e : entries) key.push_back((uintptr_t)e);
-  PtrSlot* slot = nullptr;
-  st = acquire_table(l, key, entries, stream, &slot);
+  std::vector<void*> entries;
+  tide_status_t st = rs_tables(l, -1, grads, shards, &key, &entries);
   if (st != TIDE_OK) return st;
+  return run_rs(l, 0, (int64_t)l->rs_tiles.size(), key, entries, scale, stream);
+}
 
-  RsArgs a;
-  a.tiles = l->d_rs_tiles;
-  a.num_tiles = (int64_t)l->rs_tiles.size();
-  a.gtab = (const uint16_t* const*)slot->d_table;
-  a.stab = (float* const*)(slot->d_table + (size_t)N * P);
-  a.num_ranks = N;
-  a.num_params = P;
-  a.scale = scale;
-  cudaError_t e = launch_rs(a, rs_grid(l), l->mode == TIDE_MODE_CAPPED, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter kernel launch");
-  return mark_used(l, slot, stream);
+tide_status_t tide_rs_bf16_to_fp32_rank(tide_layout_t l, int32_t rank, const uint16_t* const* grads,
+                                        float* const* shards, float scale, cudaStream_t stream) {
+  if (!l) return set_error(TIDE_ERR_INVALID_ARG, "layout is NULL");
+  if (rank < 0 || rank >= l->num_ranks) return set_error(TIDE_ERR_INVALID_ARG, "rank out of range");
+  if (l->num_params > 0 && (!grads || !shards))
+    return set_error(TIDE_ERR_INVALID_ARG, "pointer table is NULL");
+  std::lock_guard<std::mutex> g(l->mu);
+  if (l->mode == TIDE_MODE_COPY_ENGINE)
+    return set_error(TIDE_ERR_UNSUPPORTED, "reduce-scatter has no copy-engine mode");
+  std::vector<uintptr_t> key;
+  std::vector<void*> entries;
+  tide_status_t st = rs_tables(l, rank, grads, shards, &key, &entries);
+  if (st != TIDE_OK) return st;
+  return run_rs(l, l->rs_rank_begin[rank], l->rs_rank_begin[rank + 1], key, entries, scale, stream);
 }
 
 tide_status_t tide_ag_place(tide_layout_t l, const uint16_t* gathered, uint16_t* const* params,
@@ -316,8 +362,52 @@ tide_status_t tide_ag_place(tide_layout_t l, const uint16_t* gathered, uint16_t*
   a.num_tiles = (int64_t)l->ag_tiles.size();
   a.buf = gathered;
   a.ptab = (uint16_t* const*)slot->d_table;
-  cudaError_t e = launch_ag(a, ag_grid(l), l->mode == TIDE_MODE_CAPPED, stream);
+  cudaError_t e = launch_ag(a, grid_of(l, a.num_tiles, l->ag_occ), l->mode == TIDE_MODE_CAPPED, stream);
   if (e != cudaSuccess) return cuda_fail(e, "placement kernel launch");
+  return mark_used(l, slot, stream);
+}
+
+tide_status_t tide_ag_pack_bf16(tide_layout_t l, int32_t rank, const float* const* shards,
+                                uint16_t* gathered, cudaStream_t stream) {
+  if (!l) return set_error(TIDE_ERR_INVALID_ARG, "layout is NULL");
+  const int32_t N = l->num_ranks, P = l->num_params;
+  if (rank < -1 || rank >= N) return set_error(TIDE_ERR_INVALID_ARG, "rank out of range");
+  if (P > 0 && !shards) return set_error(TIDE_ERR_INVALID_ARG, "shards table is NULL");
+  std::lock_guard<std::mutex> g(l->mu);
+  if (l->mode == TIDE_MODE_COPY_ENGINE)
+    return set_error(TIDE_ERR_UNSUPPORTED, "the pack casts on the SMs; no copy-engine mode");
+  tide_status_t st = check_ptr(gathered, l->block_numel * N, "gathered", 0);
+  if (st != TIDE_OK) return st;
+  const int64_t nin = rank < 0 ? (int64_t)N * P : P;
+  for (int64_t i = 0; i < nin; ++i) {
+    st = check_ptr(shards[i], l->shard_numel[i % P], "shards", i);
+    if (st != TIDE_OK) return st;
+  }
+  const int64_t t0 = rank < 0 ? 0 : l->pk_rank_begin[rank];
+  const int64_t t1 = rank < 0 ? (int64_t)l->pk_tiles.size() : l->pk_rank_begin[rank + 1];
+  if (t1 <= t0) return TIDE_OK;
+  st = ensure_device(l);
+  if (st != TIDE_OK) return st;
+
+  std::vector<void*> entries((size_t)N * P, nullptr);
+  for (int64_t i = 0; i < nin; ++i) entries[(size_t)(rank < 0 ? i : (int64_t)rank * P + i)] = (void*)shards[i];
+  std::vector<uintptr_t> key;
+  key.reserve(2 + entries.size());
+  key.push_back((uintptr_t)TIDE_OP_PACK);
+  key.push_back((uintptr_t)(intptr_t)rank);
+  for (void* e : entries) key.push_back((uintptr_t)e);
+  PtrSlot* slot = nullptr;
+  st = acquire_table(l, key, entries, stream, &slot);
+  if (st != TIDE_OK) return st;
+
+  PackArgs a;
+  a.tiles = l->d_pk_tiles + t0;
+  a.num_tiles = t1 - t0;
+  a.stab = (const float* const*)slot->d_table;
+  a.buf = gathered;
+  a.num_params = P;
+  cudaError_t e = launch_pack(a, grid_of(l, t1 - t0, l->pk_occ), l->mode == TIDE_MODE_CAPPED, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
   return mark_used(l, slot, stream);
 }
 

@@ -69,6 +69,16 @@ struct RsArgs {
   float scale;
 };
 
+// All-gather input pack: stab[r * P + p] is rank r's fp32 shard of p (only
+// the ranks being packed are read); buf is the rank-major bf16 buffer.
+struct PackArgs {
+  const Tile* tiles;
+  int64_t num_tiles;
+  const float* const* stab;
+  uint16_t* buf;
+  int32_t num_params;
+};
+
 struct AgArgs {
   const Tile* tiles;
   int64_t num_tiles;
@@ -82,11 +92,14 @@ struct AgArgs {
 // loads in flight as one SM holds.
 cudaError_t launch_rs(const RsArgs& a, int grid, bool fat, cudaStream_t stream);
 cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, cudaStream_t stream);
+cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, cudaStream_t stream);
 int rs_block(bool fat);
 int ag_block(bool fat);
+int pk_block(bool fat);
 // Resident CTAs per SM of each kernel for `num_ranks` (RS) at its block size.
 cudaError_t rs_occupancy(int32_t num_ranks, int* blocks_per_sm);
 cudaError_t ag_occupancy(int* blocks_per_sm);
+cudaError_t pk_occupancy(int* blocks_per_sm);
 size_t rs_smem_bytes(int32_t num_ranks);
 
 // Device-side pointer table, cached by content.
@@ -111,7 +124,10 @@ struct tide_layout_s {
   int64_t align = 8;
   std::vector<int64_t> d0, inner, chunk, shard_numel, offset;
   int64_t block_numel = 0;  // S
-  std::vector<tide::Tile> rs_tiles, ag_tiles;
+  // RS and pack tiles are rank-major: rank r's tiles are
+  // [rank_begin[r], rank_begin[r + 1]) of their list.
+  std::vector<tide::Tile> rs_tiles, ag_tiles, pk_tiles;
+  std::vector<int64_t> rs_rank_begin, pk_rank_begin;
   tide_mode_t mode = TIDE_MODE_UNCAPPED;
   int32_t cta_cap = 0;
 
@@ -119,8 +135,9 @@ struct tide_layout_s {
   int device = -1;
   tide::Tile* d_rs_tiles = nullptr;
   tide::Tile* d_ag_tiles = nullptr;
+  tide::Tile* d_pk_tiles = nullptr;
   int num_sms = 0;
-  int rs_occ = 0, ag_occ = 0;
+  int rs_occ = 0, ag_occ = 0, pk_occ = 0;
   int max_pitch = 0;
   tide::PtrSlot slots[tide::kPtrSlots];
   uint64_t use_counter = 0;
@@ -130,6 +147,5 @@ struct tide_layout_s {
 namespace tide {
 tide_status_t set_error(tide_status_t st, const std::string& msg);
 tide_status_t cuda_fail(cudaError_t e, const char* what);
-int rs_grid(const tide_layout_s* l);
-int ag_grid(const tide_layout_s* l);
+int grid_of(const tide_layout_s* l, int64_t tiles, int occ);
 }  // namespace tide

@@ -49,6 +49,12 @@ class Layout:
     def reduce_scatter(self, grads, shards, scale: float, stream=None) -> None:
         _t.tide_rs_bf16_to_fp32(self.handle, grads, shards, scale, stream)
 
+    def reduce_scatter_rank(self, rank: int, grads, shards, scale: float, stream=None) -> None:
+        _t.tide_rs_bf16_to_fp32_rank(self.handle, rank, grads, shards, scale, stream)
+
+    def pack(self, rank: int, shards, gathered, stream=None) -> None:
+        _t.tide_ag_pack_bf16(self.handle, rank, shards, gathered, stream)
+
     def place(self, gathered, params, stream=None) -> None:
         _t.tide_ag_place(self.handle, gathered, params, stream)
 

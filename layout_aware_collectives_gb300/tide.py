@@ -34,6 +34,7 @@ TIDE_MODE_COPY_ENGINE = 2
 
 TIDE_OP_RS = 0
 TIDE_OP_AG = 1
+TIDE_OP_PACK = 2
 
 TIDE_MAX_RANKS = 4096
 TIDE_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -73,6 +74,8 @@ _sig("tide_layout_tiles", _st, _vp, ctypes.c_int, _vp, ctypes.c_int64, _i64p)
 _sig("tide_rs_bf16_to_fp32", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
 _sig("tide_ag_place", _st, _vp, _vp, _vp, _vp)
 _sig("tide_rs_bf16_to_fp32_noalloc", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
+_sig("tide_rs_bf16_to_fp32_rank", _st, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_float, _vp)
+_sig("tide_ag_pack_bf16", _st, _vp, ctypes.c_int32, _vp, _vp, _vp)
 _sig("tide_status_string", ctypes.c_char_p, _st)
 _sig("tide_last_error", ctypes.c_char_p)
 
@@ -238,6 +241,20 @@ def tide_rs_bf16_to_fp32_noalloc(layout, grads, shards, scale: float, stream=Non
     g, s = _table(grads), _table(shards)
     _check(_lib.tide_rs_bf16_to_fp32_noalloc(layout, _tptr(g), _tptr(s), scale, _stream(stream)),
            "tide_rs_bf16_to_fp32_noalloc")
+
+
+def tide_rs_bf16_to_fp32_rank(layout, rank: int, grads, shards, scale: float, stream=None) -> None:
+    """grads: N*P rank-major pointers; shards: the P fp32 shards of rank `rank`."""
+    g, s = _table(grads), _table(shards)
+    _check(_lib.tide_rs_bf16_to_fp32_rank(layout, rank, _tptr(g), _tptr(s), scale, _stream(stream)),
+           "tide_rs_bf16_to_fp32_rank")
+
+
+def tide_ag_pack_bf16(layout, rank: int, shards, gathered, stream=None) -> None:
+    """rank >= 0: shards = that rank's P fp32 shards; rank == -1: all N*P."""
+    s = _table(shards)
+    _check(_lib.tide_ag_pack_bf16(layout, rank, _tptr(s), _addr(gathered), _stream(stream)),
+           "tide_ag_pack_bf16")
 
 
 def tide_ag_place(layout, gathered, params, stream=None) -> None:

@@ -22,6 +22,7 @@ STREAM_GRAD = 1
 STREAM_GATHER = 2
 STREAM_ZERO = 3
 STREAM_SWEEP = 4
+STREAM_SHARD = 5
 
 #: bf16 quiet-NaN payload written into every padding / alignment slot of a
 #: gathered buffer; it must never reach a parameter.
@@ -52,6 +53,9 @@ def host_lib():
         lib.synth_gather_bf16_host.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                                ctypes.c_uint64, ctypes.c_float, ctypes.c_uint32,
                                                ctypes.c_float]
+        lib.synth_fill_f32_host.restype = None
+        lib.synth_fill_f32_host.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64,
+                                            ctypes.c_uint64, ctypes.c_float]
         _host = lib
     return _host
 
@@ -69,6 +73,9 @@ def device_lib():
         lib.synth_set_u16_device.restype = ctypes.c_int
         lib.synth_set_u16_device.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint16,
                                              ctypes.c_void_p]
+        lib.synth_fill_f32_device.restype = ctypes.c_int
+        lib.synth_fill_f32_device.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64,
+                                              ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p]
         _dev = lib
     return _dev
 
@@ -181,6 +188,17 @@ class Workload:
         if n:
             host_lib().synth_fill_bf16_host(out.ctypes.data, n, self.gather_key(p), 0,
                                             amp(self.sigma), 0, 1.0)
+        return out
+
+    def shard_key(self, rank: int, p: int) -> int:
+        return key(self.seed, STREAM_SHARD, rank, p)
+
+    def host_shard_f32(self, rank: int, p: int, n: int) -> np.ndarray:
+        """fp32 values of rank `rank`'s shard of p (pack inputs), n elements."""
+        out = np.zeros(n, dtype=np.float32)
+        if n:
+            host_lib().synth_fill_f32_host(out.ctypes.data, n, self.shard_key(rank, p), 0,
+                                           amp(self.sigma))
         return out
 
     def host_param_value_at(self, p: int, idx: np.ndarray) -> np.ndarray:

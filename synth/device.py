@@ -40,6 +40,12 @@ def fill_bf16(t: torch.Tensor, key: int, first: int, sigma: float, outlier_every
                                                outlier_every, outlier_mult, s), "synth fill")
 
 
+def fill_f32(t: torch.Tensor, key: int, first: int, sigma: float, stream=None):
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    _check(device_lib().synth_fill_f32_device(t.data_ptr(), t.numel(), key, first, amp(sigma), s),
+           "synth fill f32")
+
+
 class DeviceJob:
     def __init__(self, wl: Workload, layout, device="cuda", guard=True, fill=True, align=8):
         self.wl = wl
@@ -89,6 +95,24 @@ class DeviceJob:
                 if v:
                     dst = self.gathered[r * self.S + o: r * self.S + o + v]
                     fill_bf16(dst, wl.gather_key(p), r * c * inner, wl.sigma)
+
+    def make_pack_inputs(self):
+        """fp32 shards filled from the generator (inputs of the AG pack),
+        separate from the reduce-scatter outputs."""
+        self.pack_src = [[torch.empty(n, dtype=torch.float32, device=self.device)
+                          for n in self.shard_numel] for _ in range(self.N)]
+        for r in range(self.N):
+            for p in range(self.P):
+                t = self.pack_src[r][p]
+                if t.numel():
+                    fill_f32(t, self.wl.shard_key(r, p), 0, self.wl.sigma)
+        self.packed = torch.full((self.N * self.S,), _i16(SENTINEL_BF16), dtype=torch.int16,
+                                 device=self.device)
+
+    def pack_src_ptrs(self, rank=None):
+        if rank is None:
+            return [self.pack_src[r][p] for r in range(self.N) for p in range(self.P)]
+        return [self.pack_src[rank][p] for p in range(self.P)]
 
     # pointer lists in the ABI's order
     def grad_ptrs(self):

@@ -38,6 +38,7 @@
 #define SYNTH_STREAM_GATHER 2u   /* full parameter value behind the AG buffer */
 #define SYNTH_STREAM_ZERO 3u     /* per (rank, expert) unrouted decision     */
 #define SYNTH_STREAM_SWEEP 4u    /* rank-sweep shape draws                   */
+#define SYNTH_STREAM_SHARD 5u    /* fp32 shard values (pack inputs)          */
 #define SYNTH_OUTLIER_SALT 0xD1B54A32D192ED03ull
 
 SYNTH_FN uint64_t synth_mix64(uint64_t z) {
@@ -98,6 +99,16 @@ SYNTH_FN uint16_t synth_bf16(uint64_t key, uint64_t idx, float amp,
       synth_hash(key ^ SYNTH_OUTLIER_SALT, idx) % (uint64_t)outlier_every == 0ull)
     v = synth_mul(v, outlier_mult);
   return synth_bf16_rne(v);
+}
+
+/* fp32 element idx of the tensor with key `key`: the same Irwin-Hall draw
+ * without the bf16 rounding, so all 24 mantissa bits vary (inputs of the
+ * fp32 -> bf16 pack). */
+SYNTH_FN float synth_f32(uint64_t key, uint64_t idx, float amp) {
+  uint64_t h = synth_hash(key, idx);
+  int32_t s = (int32_t)(h & 0xFFFFu) + (int32_t)((h >> 16) & 0xFFFFu) +
+              (int32_t)((h >> 32) & 0xFFFFu) + (int32_t)(h >> 48);
+  return synth_mul((float)(2 * s - 262140), amp);
 }
 
 #endif /* TIDE_SYNTH_H */

@@ -17,6 +17,13 @@ __global__ void synth_fill_kernel(uint16_t* __restrict__ out, int64_t n, uint64_
     out[i] = synth_bf16(key, first + (uint64_t)i, amp, outlier_every, outlier_mult);
 }
 
+__global__ void synth_fill_f32_kernel(float* __restrict__ out, int64_t n, uint64_t key,
+                                      uint64_t first, float amp) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    out[i] = synth_f32(key, first + (uint64_t)i, amp);
+}
+
 __global__ void synth_set_u16_kernel(uint16_t* __restrict__ out, int64_t n, uint16_t v) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
@@ -42,6 +49,14 @@ SYNTH_EXPORT int synth_fill_bf16_device(uint16_t* out, int64_t n, uint64_t key, 
   if (n <= 0) return 0;
   synth_fill_kernel<<<grid_for(n), 256, 0, (cudaStream_t)stream>>>(out, n, key, first, amp,
                                                                   outlier_every, outlier_mult);
+  return (int)cudaGetLastError();
+}
+
+// out[i] = synth_f32(key, first + i, amp) for i in [0, n), on `stream`.
+SYNTH_EXPORT int synth_fill_f32_device(float* out, int64_t n, uint64_t key, uint64_t first, float amp,
+                                       void* stream) {
+  if (n <= 0) return 0;
+  synth_fill_f32_kernel<<<grid_for(n), 256, 0, (cudaStream_t)stream>>>(out, n, key, first, amp);
   return (int)cudaGetLastError();
 }
 

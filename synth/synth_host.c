@@ -31,3 +31,8 @@ void synth_gather_bf16_host(uint16_t* out, const int64_t* idx, int64_t n, uint64
   for (int64_t i = 0; i < n; ++i)
     out[i] = synth_bf16(key, (uint64_t)idx[i], amp, outlier_every, outlier_mult);
 }
+
+/* out[i] = synth_f32(key, first + i, amp) for i in [0, n). */
+void synth_fill_f32_host(float* out, int64_t n, uint64_t key, uint64_t first, float amp) {
+  for (int64_t i = 0; i < n; ++i) out[i] = synth_f32(key, first + (uint64_t)i, amp);
+}

@@ -186,3 +186,63 @@ def torch_check_ag(job):
             parts.append(job.gathered[r * job.S + o: r * job.S + o + v])
         want = torch.cat(parts) if parts else job.params[p][:0]
         assert torch.equal(job.params[p], want), f"placement vs torch: param {p}"
+
+
+# ---------------------------------------------------------------- single-rank RS and AG input pack
+def guarded(n, dtype, device, canary):
+    """A device buffer of n elements inside 256-byte canary bands."""
+    g = 256 // torch.tensor([], dtype=dtype).element_size()
+    buf = torch.full((n + 2 * g,), canary, dtype=dtype, device=device)
+    return buf, buf[g: g + n], g
+
+
+def check_rank_rs(job, rank, outs, scale=None):
+    """Rank `rank`'s shards bit-exact against the oracle's single-rank RS."""
+    wl = job.wl
+    scale = wl.scale if scale is None else scale
+    grads = [[wl.host_grad(k, p) for p in range(job.P)] for k in range(job.N)]
+    want = oracle.rs_rank(wl.shapes, job.N, grads, scale, rank)
+    for p in range(job.P):
+        got = _bits32(outs[p])
+        assert np.array_equal(got, want[p].view(np.uint32)), f"rank RS: rank {rank} param {p}"
+
+
+def host_pack(job, ranks):
+    """The oracle's pack of host-regenerated fp32 shards into a sentinel buffer."""
+    wl = job.wl
+    offs, S = oracle.layout(wl.shapes, job.N, job.align)
+    buf = np.full(job.N * S, SENTINEL_BF16, dtype=np.uint16)
+    for r in ranks:
+        src = [wl.host_shard_f32(r, p, job.shard_numel[p]) for p in range(job.P)]
+        oracle.ag_pack(wl.shapes, job.N, offs, S, r, src, buf)
+    return buf
+
+
+def check_pack(job, ranks):
+    got = _bits16(job.packed)
+    want = host_pack(job, ranks)
+    if not np.array_equal(got, want):
+        bad = np.flatnonzero(got != want)
+        raise AssertionError(f"pack mismatch at {bad.size} slots, first {bad[0]}: "
+                             f"got {got[bad[0]]:04x} want {want[bad[0]]:04x}")
+
+
+def sampled_check_pack(job, seed=0, per=16):
+    """Sampled slots of every (rank, param) block against the oracle rounding."""
+    wl = job.wl
+    rng = np.random.default_rng(seed)
+    offs, S = oracle.layout(wl.shapes, job.N, job.align)
+    checked = 0
+    for p in range(job.P):
+        n = job.shard_numel[p]
+        if n == 0:
+            continue
+        for r in range(job.N):
+            idx = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, size=per)]))
+            src = wl.host_shard_f32(r, p, int(idx.max()) + 1)[idx]
+            want = oracle.f32_to_bf16(src)
+            pos = torch.from_numpy(r * S + offs[p] + idx).to(job.device)
+            got = _bits16(job.packed[pos])
+            assert np.array_equal(got, want), f"pack param {p} rank {r}"
+            checked += idx.size
+    return checked

@@ -199,3 +199,63 @@ def test_empty_layout_calls_are_noops_without_a_device():
         lay.reduce_scatter([], [], 1.0)
         lay.place(None, [])
         assert len(lay.tiles(tide.TIDE_OP_RS)) == 0
+
+
+@pytest.mark.parametrize("n,shapes,align", [
+    (4, [(256, 256), (704, 256), (256, 704), (250,)], 8),
+    (3, [(5, 3), (1,), (), (0, 4), (17, 9)], 1),
+    (64, [(1000, 4096), (63, 4096)], 8),
+])
+def test_pack_tiles_partition_and_rank_order(n, shapes, align):
+    """Pack tiles cover every element of every padded shard exactly once at
+    r*S + o_p + e; RS and pack lists are rank-major (single-rank calls use a
+    contiguous sub-range)."""
+    offs, S = oracle.layout(shapes, n, align)
+    with tide.Layout(shapes, n, align_elems=align) as lay:
+        pk = lay.tiles(tide.TIDE_OP_PACK)
+        rs = lay.tiles(tide.TIDE_OP_RS)
+    for lst in (pk, rs):
+        if len(lst):
+            assert np.all(np.diff(lst[:, 1]) >= 0)
+    cover = {}
+    for p, r, src, dst, ln, flags in pk:
+        d0, inner = _dims(shapes[p])
+        c = oracle.chunk_rows(d0, n)
+        cnt = cover.setdefault((p, r), np.zeros(c * inner, dtype=np.int64))
+        cnt[src: src + ln] += 1
+        assert dst == r * S + offs[p] + src
+        if flags & 2:
+            assert src % 4 == 0 and dst % 8 == 0
+    for p, s in enumerate(shapes):
+        d0, inner = _dims(s)
+        if oracle.chunk_rows(d0, n) * inner:
+            for r in range(n):
+                assert np.all(cover[(p, r)] == 1), (p, r)
+
+
+def test_rank_and_pack_calls_validate_on_the_host():
+    shapes = [(8, 2), (5,)]
+    good = 0x10000
+    with tide.Layout(shapes, 2) as lay:
+        grads = [good + 0x1000 * i for i in range(4)]
+        mine = [good + 0x8000, good + 0x9000]
+        for bad_rank in (-1, 2):
+            with pytest.raises(tide.TideError) as e:
+                lay.reduce_scatter_rank(bad_rank, grads, mine, 0.5)
+            assert e.value.status == tide.TIDE_ERR_INVALID_ARG
+        with pytest.raises(tide.TideError) as e:
+            lay.pack(2, mine, good)
+        assert e.value.status == tide.TIDE_ERR_INVALID_ARG
+        with pytest.raises(tide.TideError) as e:
+            lay.pack(0, [good + 4, good], good)
+        assert e.value.status == tide.TIDE_ERR_MISALIGNED
+        with pytest.raises(tide.TideError) as e:
+            lay.pack(-1, mine + [None, good], good)  # all-rank form: N*P pointers, one NULL
+        assert e.value.status == tide.TIDE_ERR_INVALID_ARG
+        lay.set_mode(tide.TIDE_MODE_COPY_ENGINE)
+        with pytest.raises(tide.TideError) as e:
+            lay.pack(0, mine, good)
+        assert e.value.status == tide.TIDE_ERR_UNSUPPORTED
+        with pytest.raises(tide.TideError) as e:
+            lay.reduce_scatter_rank(0, grads, mine, 0.5)
+        assert e.value.status == tide.TIDE_ERR_UNSUPPORTED

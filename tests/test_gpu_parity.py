@@ -135,6 +135,64 @@ def test_ragged_shapes_full_parity(case, align):
             assert job.guards_intact()
 
 
+def _rank_rs_and_pack(job, modes, scale=None):
+    scale = job.wl.scale if scale is None else scale
+    job.make_pack_inputs()
+    for mode in modes:
+        job.layout.set_mode(*mode[1:])
+        for r in range(job.N):
+            bufs = [gpu_checks.guarded(n, torch.int32, job.device, -0x5A5A5A5B)
+                    for n in job.shard_numel]
+            outs = [b[1].view(torch.float32) for b in bufs]
+            job.layout.reduce_scatter_rank(r, job.grad_ptrs(), outs, scale)
+            torch.cuda.synchronize()
+            gpu_checks.check_rank_rs(job, r, outs, scale)
+            for buf, view, g in bufs:
+                assert bool((buf[:g] == -0x5A5A5A5B).all()) and bool((buf[g + view.numel():] == -0x5A5A5A5B).all())
+        # pack rank by rank (each call writes only its own block), then all at once
+        job.packed.fill_(0x7FC1)
+        for r in range(job.N):
+            job.layout.pack(r, job.pack_src_ptrs(r), job.packed)
+            torch.cuda.synchronize()
+            gpu_checks.check_pack(job, range(r + 1))
+        job.packed.fill_(0x7FC1)
+        job.layout.pack(-1, job.pack_src_ptrs(), job.packed)
+        torch.cuda.synchronize()
+        gpu_checks.check_pack(job, range(job.N))
+
+
+@pytest.mark.parametrize("mode", MODES, ids=[m[0] for m in MODES])
+def test_tiny_rank_rs_and_pack(tiny_job, mode):
+    _rank_rs_and_pack(tiny_job, [mode])
+
+
+@pytest.mark.parametrize("align", [8, 1])
+@pytest.mark.parametrize("case", _ragged_cases(), ids=lambda c: f"N{c[0]}")
+def test_ragged_rank_rs_and_pack(case, align):
+    n, shapes = case
+    wl = synth.custom(f"ragged{n}", n, shapes, sigma=0.5, seed=n)
+    with tide.Layout(wl.shapes, n, align_elems=align) as lay:
+        job = DeviceJob(wl, lay, align=align)
+        _rank_rs_and_pack(job, MODES[:2], scale=0.3)
+
+
+def test_pack_special_values():
+    """Ties, overflow, subnormals, infinities and NaNs through the device pack."""
+    bits = np.array([0x3F800000, 0x3F808000, 0x3F818000, 0x3F808001, 0x3F807FFF, 0xBF818000,
+                     0x7F7FFFFF, 0x7F7F7FFF, 0x80000000, 0x00000001, 0x00008000, 0x00018000,
+                     0x7F800000, 0xFF800000, 0x7FC00000, 0x7F800001, 0xFFC00001, 0x00000000],
+                    dtype=np.uint32)
+    n = bits.size
+    with tide.Layout([(n,)], 1) as lay:
+        src = torch.from_numpy(bits.view(np.int32).copy()).cuda().view(torch.float32)
+        out = torch.zeros(lay.block_numel, dtype=torch.int16, device="cuda")
+        lay.pack(0, [src], out)
+        torch.cuda.synchronize()
+        got = out[:n].cpu().numpy().view(np.uint16)
+        import oracle
+        assert np.array_equal(got, oracle.f32_to_bf16(bits.view(np.float32)))
+
+
 def test_empty_layout():
     with tide.Layout([], 4) as lay:
         lay.reduce_scatter([], [], 0.25)
@@ -164,6 +222,18 @@ def test_full_size_sampled_parity(name):
         assert gpu_checks.sampled_check_ag(job) > 0
         gpu_checks.torch_check_rs(job)
         gpu_checks.torch_check_ag(job)
+        for r in (0, job.N - 1):
+            outs = [torch.empty(n, dtype=torch.float32, device="cuda") for n in job.shard_numel]
+            lay.reduce_scatter_rank(r, job.grad_ptrs(), outs, wl.scale)
+            torch.cuda.synchronize()
+            for p in range(job.P):
+                assert torch.equal(outs[p].view(torch.int32), job.shards[r][p].view(torch.int32)), (r, p)
+            del outs
+        job.make_pack_inputs()
+        lay.pack(-1, job.pack_src_ptrs(), job.packed)
+        torch.cuda.synchronize()
+        assert gpu_checks.sampled_check_pack(job) > 0
+        del job.pack_src, job.packed
         ref = [s.clone() for s in (job.shards[0][0], job.shards[-1][-1])]
         lay.set_mode(tide.TIDE_MODE_CAPPED, 64)
         for row in job.shards:

@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--no-interference", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stock", action="store_true")
     return ap.parse_args()
 
 
@@ -407,6 +408,8 @@ def run_tide(args):
     }
 
     out["next_ops"] = run_next_ops(tide, layout, job, wl, stream)
+    if not args.no_stock:
+        out["stock_fsdp2"] = run_stock(job, wl, stream, rs_avg, ag_avg)
     if not args.no_e2e:
         out["e2e"] = run_e2e(tide, layout, job, wl, stream, K, world)
     if not args.no_interference:
@@ -458,6 +461,110 @@ def run_next_ops(tide, layout, job, wl, stream, reps=20):
         res[name] = {"ms": round(ms, 4), "bytes": nbytes,
                      "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
     del outs, job.pack_src, job.packed
+    return res
+
+
+# ---------------------------------------------------------------- stock FSDP2 emulation
+class StockFSDP2:
+    """What stock FSDP2 does around its collectives, in the PyTorch ops it
+    uses, on the same N simulated ranks: the reduce-scatter input is built by
+    copying every rank's per-parameter bf16 gradients into one flat fp32
+    rank-major buffer (torch._chunk_cat with a cast, dense dim-0 chunks, zero
+    padding); the reduction then runs on the flat buffers (here a rank-order
+    fp32 sum, on the wire in a real job); the all-gather output, a flat bf16
+    rank-major buffer, is copied out into padded per-parameter storage
+    (torch.split_with_sizes_copy).  The copy-in and copy-out are the layout
+    conversion ("FSDP通信终局：TIDE零拷贝集合通信优化" §FSDP2通信开销的根源) that
+    TIDE's fused reduce-scatter and direct placement avoid."""
+
+    def __init__(self, job):
+        import torch
+
+        self.job = job
+        N = job.N
+        self.sizes = list(job.shard_numel)            # c_p * inner_p
+        self.S1 = sum(self.sizes)                      # dense rank block
+        self.offs1 = [sum(self.sizes[:p]) for p in range(job.P)]
+        dev = job.device
+        self.flat = [torch.empty(N, self.S1, dtype=torch.float32, device=dev) for _ in range(N)]
+        self.out = torch.empty(N * self.S1, dtype=torch.float32, device=dev)
+        self.gathered = torch.zeros(N, self.S1, dtype=torch.bfloat16, device=dev)
+        self.padded = [torch.empty(N * n, dtype=torch.bfloat16, device=dev) for n in self.sizes]
+        # the stock all-gather output holds the same chunks as TIDE's buffer
+        for p in range(job.P):
+            o, o1, n = job.layout.param_offset(p), self.offs1[p], self.sizes[p]
+            for r in range(N):
+                self.gathered[r, o1:o1 + n] = job.gathered[r * job.S + o: r * job.S + o + n].view(torch.bfloat16)
+        self.grad_views = [[self._view(job.grads[k][p], job.wl.shapes[p]) for p in range(job.P)]
+                           for k in range(N)]
+
+    @staticmethod
+    def _view(t, shape):
+        import torch
+
+        shp = tuple(shape) if len(shape) else (1,)
+        return t.view(torch.bfloat16).view(shp)
+
+    def copy_in(self):
+        import torch
+
+        for k in range(self.job.N):
+            torch._chunk_cat(self.grad_views[k], dim=0, num_chunks=self.job.N, out=self.flat[k])
+
+    def flat_reduce(self, scale):
+        self.out.zero_()
+        for k in range(self.job.N):
+            self.out.add_(self.flat[k].view(-1))
+        self.out.mul_(scale)
+
+    def copy_out(self):
+        import torch
+
+        torch.split_with_sizes_copy(self.gathered, self.sizes, dim=1,
+                                    out=[b.view(self.job.N, n) for b, n in zip(self.padded, self.sizes)])
+
+    def shard(self, r, p):
+        o1 = r * self.S1 + self.offs1[p]
+        return self.out[o1: o1 + self.sizes[p]]
+
+    def param(self, p):
+        d0, inner = self.job.dims[p]
+        return self.padded[p][: d0 * inner]
+
+
+def run_stock(job, wl, stream, tide_rs_ms, tide_ag_ms, reps=10):
+    """Times of the stock emulation's three parts next to TIDE's kernels."""
+    import torch
+
+    st = StockFSDP2(job)
+    N, psi, padded = wl.num_ranks, wl.psi, sum(job.shard_numel)
+    flat = N * padded  # elements of one rank's flat buffer (every destination block)
+    parts = {"rs_copy_in": (st.copy_in, N * (2 * psi + 4 * flat)),
+             # zero_, N rank-order add_ passes (read out + read flat_k + write out), mul_
+             "flat_reduce": (lambda: st.flat_reduce(wl.scale), 4 * flat + N * 12 * flat + 8 * flat),
+             "ag_copy_out": (st.copy_out, 4 * flat)}
+    res = {}
+    with torch.cuda.stream(stream):
+        for name, (fn, nbytes) in parts.items():
+            fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            res[name] = {"ms": round(ms, 4), "bytes": nbytes, "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    conv = res["rs_copy_in"]["ms"] + res["ag_copy_out"]["ms"]
+    total = conv + res["flat_reduce"]["ms"]
+    res["layout_conversion_ms"] = round(conv, 4)
+    res["stock_step_ms"] = round(total, 4)
+    res["tide_step_ms"] = round(tide_rs_ms + tide_ag_ms, 4)
+    res["tide_speedup_vs_stock"] = round(total / (tide_rs_ms + tide_ag_ms), 2)
+    res["note"] = ("stock = chunk_cat copy-in (bf16->fp32) + torch rank-order fp32 sum of flat "
+                   "buffers + split_with_sizes_copy copy-out; TIDE = fused RS + placement")
+    del st
+    torch.cuda.empty_cache()
     return res
 
 

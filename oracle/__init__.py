@@ -55,6 +55,14 @@ def lib():
         L.oracle_ag_pack.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_rs_stage.restype = None
+        L.oracle_rs_stage.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                      ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_rs_staged.restype = None
+        L.oracle_rs_staged.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float]
         _lib = L
     return _lib
 
@@ -180,3 +188,31 @@ def ag_pack(shapes, num_ranks: int, offsets, block_numel: int, r: int, shards_r,
     lib().oracle_ag_pack(num_ranks, P, d0.ctypes.data, inner.ctypes.data, offs.ctypes.data,
                          block_numel, r, sp.ctypes.data, gathered.ctypes.data)
     return gathered
+
+
+def rs_stage(shapes, num_ranks: int, offsets, block_numel: int, grads_k, slot):
+    """Writes rank k's gradients into `slot` (uint16, N*S, modified in place)."""
+    P = len(shapes)
+    d0, inner = _dims(shapes)
+    g = [np.ascontiguousarray(grads_k[p], dtype=np.uint16) for p in range(P)]
+    offs = np.ascontiguousarray(offsets, dtype=np.int64)
+    assert slot.dtype == np.uint16 and slot.flags.c_contiguous
+    gp = _ptrs(g)
+    lib().oracle_rs_stage(num_ranks, P, d0.ctypes.data, inner.ctypes.data, offs.ctypes.data,
+                          block_numel, gp.ctypes.data, slot.ctypes.data)
+    return slot
+
+
+def rs_staged(shapes, num_ranks: int, offsets, block_numel: int, slots, scale: float):
+    """Reduce-scatter from N staged slots; returns shards[r][p]."""
+    P = len(shapes)
+    d0, inner = _dims(shapes)
+    sl = [np.ascontiguousarray(x, dtype=np.uint16) for x in slots]
+    offs = np.ascontiguousarray(offsets, dtype=np.int64)
+    shards = [[np.empty(chunk_rows(int(d0[p]), num_ranks) * int(inner[p]), dtype=np.float32)
+               for p in range(P)] for _ in range(num_ranks)]
+    flat = [shards[r][p] for r in range(num_ranks) for p in range(P)]
+    sp, op = _ptrs(sl), _ptrs(flat)
+    lib().oracle_rs_staged(num_ranks, P, d0.ctypes.data, inner.ctypes.data, offs.ctypes.data,
+                           block_numel, sp.ctypes.data, op.ctypes.data, scale)
+    return shards

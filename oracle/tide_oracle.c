@@ -142,3 +142,38 @@ void oracle_ag_pack(int32_t num_ranks, int32_t num_params, const int64_t* d0, co
       gathered[(int64_t)r * block_numel + offsets[p] + e] = oracle_f32_to_bf16(shards_r[p][e]);
   }
 }
+
+void oracle_rs_stage(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                     const int64_t* offsets, int64_t block_numel, const uint16_t* const* grads_k,
+                     uint16_t* slot) {
+  for (int32_t p = 0; p < num_params; ++p) {
+    const int64_t c = oracle_chunk_rows(d0[p], num_ranks);
+    for (int32_t r = 0; r < num_ranks; ++r) {
+      const int64_t n = oracle_valid_rows(d0[p], num_ranks, r) * inner[p];
+      for (int64_t e = 0; e < n; ++e)
+        slot[(int64_t)r * block_numel + offsets[p] + e] = grads_k[p][(int64_t)r * c * inner[p] + e];
+    }
+  }
+}
+
+void oracle_rs_staged(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                      const int64_t* offsets, int64_t block_numel, const uint16_t* const* slots,
+                      float* const* shards, float scale) {
+  uint16_t vals[4096];
+  for (int32_t p = 0; p < num_params; ++p) {
+    const int64_t c = oracle_chunk_rows(d0[p], num_ranks);
+    for (int32_t r = 0; r < num_ranks; ++r) {
+      float* out = shards[(int64_t)r * num_params + p];
+      const int64_t n = oracle_valid_rows(d0[p], num_ranks, r) * inner[p];
+      for (int64_t e = 0; e < c * inner[p]; ++e) {
+        if (e < n) {
+          for (int32_t k = 0; k < num_ranks; ++k)
+            vals[k] = slots[k][(int64_t)r * block_numel + offsets[p] + e];
+          out[e] = oracle_rs_element(num_ranks, vals, scale);
+        } else {
+          out[e] = 0.0f;
+        }
+      }
+    }
+  }
+}

@@ -95,6 +95,23 @@ void oracle_ag_pack(int32_t num_ranks, int32_t num_params, const int64_t* d0, co
                     const int64_t* offsets, int64_t block_numel, int32_t r,
                     const float* const* shards_r, uint16_t* gathered);
 
+/* Slot-Reuse staging of rank k's gradients ([TIDE] "TIDE的设计思路": the
+ * vacated all-gather slot holds the gradients): the slot has the rank-major
+ * layout of the gathered buffer and receives, for every destination rank r,
+ * the rows of each gradient that r owns:
+ *   slot[r * S + o_p + e] = grad_k[p][r * c_p * inner[p] + e]  for e < v_{p,r} * inner[p].
+ * Padding and alignment slots are untouched. */
+void oracle_rs_stage(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                     const int64_t* offsets, int64_t block_numel, const uint16_t* const* grads_k,
+                     uint16_t* slot);
+
+/* Reduce-scatter from the N staged slots:
+ *   shards[r * P + p][e] = scale * sum_{k=0}^{N-1} f32(slots[k][r * S + o_p + e])  for e < v_{p,r} * inner[p],
+ *   +0.0f for the padding rows; fp32 sum in ascending k from +0.0f. */
+void oracle_rs_staged(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                      const int64_t* offsets, int64_t block_numel, const uint16_t* const* slots,
+                      float* const* shards, float scale);
+
 #ifdef __cplusplus
 }
 #endif

@@ -400,3 +400,48 @@ def check_pack_then_place(seed=10):
 
 ALL_CHECKS += [check_bf16_rounding_golden, check_bf16_rounding_vs_torch, check_rs_rank_matches_full,
                check_pack_then_place]
+
+
+# ---------------------------------------------------------------- Slot-Reuse staged reduce-scatter
+def check_stage_is_inverse_of_placement(seed=11):
+    """Staging a full gradient into the rank-major slot and placing the slot
+    back gives the gradient (bit for bit); every padding slot keeps the
+    sentinel."""
+    rng = np.random.default_rng(seed)
+    for n in (1, 2, 3, 5):
+        for align in (1, 8):
+            shapes = [(int(rng.integers(1, 3 * n + 4)), int(rng.integers(1, 6))) for _ in range(3)]
+            shapes += [(n - 1 if n > 1 else 1,), (4, 2, 3)]
+            g = [random_bf16(rng, dims(s)[0] * dims(s)[1]) for s in shapes]
+            for x in g:
+                x[x == SENTINEL] = 0x3F80
+            offs, S = oracle.layout(shapes, n, align)
+            slot = np.full(n * S, SENTINEL, dtype=np.uint16)
+            oracle.rs_stage(shapes, n, offs, S, g, slot)
+            # the slot is exactly the rank-major packing of the gradient
+            assert np.array_equal(slot, pack_rank_major(shapes, n, g, offs, S))
+            back = oracle.ag_place(shapes, n, slot, offs, S)
+            for p in range(len(shapes)):
+                assert np.array_equal(back[p], g[p]), (n, align, p)
+
+
+def check_staged_rs_equals_rs(seed=12):
+    """Reduce-scatter from the staged slots equals the brute-force reduce-
+    scatter of the per-parameter gradients, bit for bit."""
+    rng = np.random.default_rng(seed)
+    for n in (1, 2, 4, 5, 8):
+        shapes = [(2 * n + 3, 4), (n + 1,), (3, 3, 2), (1, 7)]
+        grads = [[random_bf16(rng, dims(s)[0] * dims(s)[1]) for s in shapes] for _ in range(n)]
+        offs, S = oracle.layout(shapes, n, 8)
+        slots = []
+        for k in range(n):
+            slot = np.full(n * S, SENTINEL, dtype=np.uint16)  # padding is never read
+            slots.append(oracle.rs_stage(shapes, n, offs, S, grads[k], slot))
+        got = oracle.rs_staged(shapes, n, offs, S, slots, 1.0 / n)
+        want = brute_force_rs(shapes, n, grads, 1.0 / n)
+        for r in range(n):
+            for p in range(len(shapes)):
+                assert np.array_equal(fp32_bits(got[r][p]), fp32_bits(want[r][p])), (n, r, p)
+
+
+ALL_CHECKS += [check_stage_is_inverse_of_placement, check_staged_rs_equals_rs]

@@ -33,6 +33,10 @@ MUTANTS = {
                          "gathered[(int64_t)r * block_numel + offsets[p] + e - (e > 0 ? 1 : 0)]"),
     "rank_rs_wrong_row": ("const int64_t i = (int64_t)r * c + ii;\n      for (int64_t j = 0; j < inner[p]; ++j) {\n        if (i < d0[p]) {\n          for (int32_t k = 0; k < num_ranks; ++k)\n            vals[k] = grads[(int64_t)k * num_params + p][i * inner[p] + j];\n          shards_r",
                           "const int64_t i = (int64_t)r * c + ii + (ii + 1 < c ? 1 : 0);\n      for (int64_t j = 0; j < inner[p]; ++j) {\n        if (i < d0[p]) {\n          for (int32_t k = 0; k < num_ranks; ++k)\n            vals[k] = grads[(int64_t)k * num_params + p][i * inner[p] + j];\n          shards_r"),
+    "stage_wrong_source_row": ("slot[(int64_t)r * block_numel + offsets[p] + e] = grads_k[p][(int64_t)r * c * inner[p] + e];",
+                               "slot[(int64_t)r * block_numel + offsets[p] + e] = grads_k[p][(int64_t)r * n + e];"),
+    "staged_rs_reads_padding": ("        if (e < n) {\n          for (int32_t k = 0; k < num_ranks; ++k)\n            vals[k] = slots[k]",
+                                "        if (e < c * inner[p]) {\n          for (int32_t k = 0; k < num_ranks; ++k)\n            vals[k] = slots[k]"),
     "unaligned_offsets": ("o = roundup(o + oracle_chunk_rows(d0[p], num_ranks) * inner[p], align);",
                           "o = o + oracle_chunk_rows(d0[p], num_ranks) * inner[p];"),
 }

@@ -461,6 +461,35 @@ def run_next_ops(tide, layout, job, wl, stream, reps=20):
         res[name] = {"ms": round(ms, 4), "bytes": nbytes,
                      "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
     del outs, job.pack_src, job.packed
+    # Slot-Reuse two-stage path: stage every rank's gradients into its slot,
+    # then reduce-scatter from the slots
+    job.make_slots()
+    sptr = tide.PointerTable(job.shard_ptrs())
+    slot_tab = tide.PointerTable(job.slots)
+    gtabs = [tide.PointerTable([job.grads[k][p] for p in range(job.P)]) for k in range(N)]
+
+    def stage_all():
+        for k in range(N):
+            layout.stage(gtabs[k], job.slots[k], stream)
+
+    for name, op, nbytes in (
+            ("stage_all_ranks", stage_all, 4 * N * wl.psi),
+            ("rs_from_staged_slots", lambda: layout.reduce_scatter_staged(slot_tab, sptr, wl.scale, stream),
+             wl.rs_bytes())):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                op()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                op()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"ms": round(ms, 4), "bytes": nbytes,
+                     "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    del job.slots
+    torch.cuda.empty_cache()
     return res
 
 

@@ -95,9 +95,14 @@ typedef enum {
   TIDE_MODE_COPY_ENGINE = 2
 } tide_mode_t;
 
-/* Operations, for the launch-shape and tile-list queries: the
- * reduce-scatter, the placement and the all-gather input pack. */
-typedef enum { TIDE_OP_RS = 0, TIDE_OP_AG = 1, TIDE_OP_PACK = 2 } tide_op_t;
+/* Operations, for the launch-shape and tile-list queries. */
+typedef enum {
+  TIDE_OP_RS = 0,
+  TIDE_OP_AG = 1,
+  TIDE_OP_PACK = 2,
+  TIDE_OP_STAGE = 3,     /* Slot-Reuse staging (runs the placement list backwards) */
+  TIDE_OP_STAGED_RS = 4  /* reduce-scatter from staged slots */
+} tide_op_t;
 
 /* Maximum simulated ranks per layout. */
 #define TIDE_MAX_RANKS 4096
@@ -236,6 +241,37 @@ TIDE_API tide_status_t tide_rs_bf16_to_fp32_rank(tide_layout_t layout, int32_t r
  */
 TIDE_API tide_status_t tide_ag_pack_bf16(tide_layout_t layout, int32_t rank, const float* const* shards,
                                          uint16_t* gathered, cudaStream_t stream);
+
+/*
+ * Slot-Reuse staging ("TIDE的设计思路": the optional Slot-Reuse mechanism
+ * stages gradients in the vacated all-gather slot, and a two-stage pipeline
+ * decouples gradient reads from the collective's progress).  Copies one
+ * rank's per-parameter bf16 gradients into its slot, a buffer with the
+ * rank-major layout of the gathered buffer, destination by destination:
+ *   slot[r*S + o_p + e] = grads[p][r*c_p*inner_p + e]   for e < v_{p,r}*inner_p.
+ * Padding and alignment slots are not written.  Every rank stages the same
+ * way into its own slot.
+ *   grads  host array of P device pointers (bf16, 16-byte aligned);
+ *   slot   device pointer to N*S bf16 elements (16-byte aligned).
+ * Bit copy.  In TIDE_MODE_COPY_ENGINE the copy runs on the copy engines
+ * (the placement's 2-D copies reversed).
+ */
+TIDE_API tide_status_t tide_rs_stage_bf16(tide_layout_t layout, const uint16_t* const* grads, uint16_t* slot,
+                                          cudaStream_t stream);
+
+/*
+ * Reduce-scatter from N staged slots (the second stage of the Slot-Reuse
+ * pipeline): every rank's inputs are now one contiguous rank-major buffer.
+ *   shards[r*P + p][e] = scale * sum_{k=0}^{N-1} f32(slots[k][r*S + o_p + e])  for e < v_{p,r}*inner_p,
+ *   +0.0f in padding rows; fp32 sum in ascending k from +0.0f — bit for bit
+ *   the result of tide_rs_bf16_to_fp32 on the unstaged gradients.
+ *   slots   host array of N device pointers (N*S bf16 each, 16-byte aligned);
+ *   shards  host array of N*P device pointers, as for tide_rs_bf16_to_fp32.
+ * Padding slots of the slots are never read.  TIDE_ERR_UNSUPPORTED in
+ * TIDE_MODE_COPY_ENGINE.
+ */
+TIDE_API tide_status_t tide_rs_staged_bf16_to_fp32(tide_layout_t layout, const uint16_t* const* slots,
+                                                   float* const* shards, float scale, cudaStream_t stream);
 
 /* Bytes of the device array behind tide_rs_bf16_to_fp32_noalloc. */
 #define TIDE_NOALLOC_SCRATCH_BYTES (4u << 20)

@@ -172,13 +172,21 @@ __global__ void __launch_bounds__(THREADS, TIDE_RS_MIN_BLOCKS) rs_kernel(RsArgs 
 // ---------------------------------------------------------------- placement
 // One tile = a contiguous run of rank r's chunk of parameter p: a copy from
 // gathered[r*S + o_p + ...] to params[p][r*c_p*inner_p + ...].  U 16-byte
-// vectors per thread are loaded before any is stored.
-template <int THREADS, int U>
+// vectors per thread are loaded before any is stored.  TO_BUF runs the same
+// copy backwards (Slot-Reuse staging of a gradient into the rank-major slot).
+template <int THREADS, int U, bool TO_BUF>
 __global__ void __launch_bounds__(THREADS) ag_kernel(AgArgs a) {
   for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
-    const uint16_t* __restrict__ src = a.buf + tile.src;
-    uint16_t* __restrict__ dst = a.ptab[tile.p] + tile.dst;
+    const uint16_t* __restrict__ src;
+    uint16_t* __restrict__ dst;
+    if constexpr (TO_BUF) {
+      src = a.ptab[tile.p] + tile.dst;
+      dst = const_cast<uint16_t*>(a.buf) + tile.src;
+    } else {
+      src = a.buf + tile.src;
+      dst = a.ptab[tile.p] + tile.dst;
+    }
     if (tile.flags & kTileVec) {
       const int nvec = tile.len >> 3;
       for (int v0 = threadIdx.x; v0 < nvec; v0 += U * THREADS) {
@@ -267,8 +275,10 @@ RsKernel rs_kernel_for(int32_t n, bool fat) {
   return fat ? rs_kernel_for<kFatThreads>(n) : rs_kernel_for<kRsThreads>(n);
 }
 
-AgKernel ag_kernel_for(bool fat) {
-  return fat ? ag_kernel<kFatThreads, TIDE_AG_UNROLL> : ag_kernel<kAgThreads, TIDE_AG_UNROLL>;
+AgKernel ag_kernel_for(bool fat, bool to_buf = false) {
+  if (to_buf)
+    return fat ? ag_kernel<kFatThreads, TIDE_AG_UNROLL, true> : ag_kernel<kAgThreads, TIDE_AG_UNROLL, true>;
+  return fat ? ag_kernel<kFatThreads, TIDE_AG_UNROLL, false> : ag_kernel<kAgThreads, TIDE_AG_UNROLL, false>;
 }
 
 }  // namespace
@@ -291,6 +301,12 @@ cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, cudaStream_t stream) 
 }
 
 int pk_block(bool fat) { return fat ? kFatThreads : kAgThreads; }
+
+cudaError_t launch_stage(const AgArgs& a, int grid, bool fat, cudaStream_t stream) {
+  if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
+  ag_kernel_for(fat, true)<<<grid, ag_block(fat), 0, stream>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;

@@ -51,6 +51,7 @@ void build_tiles(tide_layout_s* l) {
   l->rs_tiles.clear();
   l->ag_tiles.clear();
   l->pk_tiles.clear();
+  l->st_tiles.clear();
   l->rs_rank_begin.assign(1, 0);
   l->pk_rank_begin.assign(1, 0);
   // rank-major: one rank's tiles are contiguous (single-rank calls launch a
@@ -72,6 +73,18 @@ void build_tiles(tide_layout_s* l) {
         l->rs_tiles.push_back(t);
       });
       const int64_t ag_src = (int64_t)r * l->block_numel + l->offset[p];
+      // staged reduce-scatter: the same runs read from every rank's slot at
+      // r*S + o_p (padding runs as above)
+      split_runs(seg, T, [&](int64_t s, int64_t n) {
+        Tile t{ag_src + s, s, (int32_t)n, p, r, 0u};
+        if (t.src % 8 == 0 && t.dst % 4 == 0) t.flags |= kTileVec;
+        l->st_tiles.push_back(t);
+      });
+      split_runs(c * inner - seg, kZeroTileElems, [&](int64_t s, int64_t n) {
+        Tile t{0, seg + s, (int32_t)n, p, r, kTileZero};
+        if (t.dst % 4 == 0) t.flags |= kTileVec;
+        l->st_tiles.push_back(t);
+      });
       split_runs(seg, kAgTileElems, [&](int64_t s, int64_t n) {
         Tile t{ag_src + s, rs_src + s, (int32_t)n, p, r, 0u};
         if (t.src % 8 == 0 && t.dst % 8 == 0) t.flags |= kTileVec;
@@ -256,10 +269,11 @@ tide_status_t tide_layout_set_mode(tide_layout_t l, tide_mode_t mode, int32_t ct
 tide_status_t tide_layout_tiles(tide_layout_t l, tide_op_t op, int64_t* rows, int64_t cap,
                                 int64_t* count) {
   if (!l || !count) return set_error(TIDE_ERR_INVALID_ARG, "NULL argument");
-  if (op != TIDE_OP_RS && op != TIDE_OP_AG && op != TIDE_OP_PACK)
-    return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
-  const std::vector<tide::Tile>& t =
-      op == TIDE_OP_RS ? l->rs_tiles : op == TIDE_OP_AG ? l->ag_tiles : l->pk_tiles;
+  if (op < TIDE_OP_RS || op > TIDE_OP_STAGED_RS) return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
+  const std::vector<tide::Tile>& t = op == TIDE_OP_RS     ? l->rs_tiles
+                                     : op == TIDE_OP_PACK ? l->pk_tiles
+                                     : op == TIDE_OP_STAGED_RS ? l->st_tiles
+                                                               : l->ag_tiles;  // AG and STAGE
   *count = (int64_t)t.size();
   if (cap > 0 && !rows) return set_error(TIDE_ERR_INVALID_ARG, "rows is NULL");
   for (int64_t i = 0; i < std::min<int64_t>(cap, (int64_t)t.size()); ++i) {

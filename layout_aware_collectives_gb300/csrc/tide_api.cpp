@@ -61,9 +61,10 @@ tide_status_t ensure_device(tide_layout_s* l) {
     const std::vector<Tile>* host;
     Tile** dev;
     const char* what;
-  } lists[3] = {{&l->rs_tiles, &l->d_rs_tiles, "reduce-scatter tile list"},
+  } lists[4] = {{&l->rs_tiles, &l->d_rs_tiles, "reduce-scatter tile list"},
                 {&l->ag_tiles, &l->d_ag_tiles, "placement tile list"},
-                {&l->pk_tiles, &l->d_pk_tiles, "pack tile list"}};
+                {&l->pk_tiles, &l->d_pk_tiles, "pack tile list"},
+                {&l->st_tiles, &l->d_st_tiles, "staged reduce-scatter tile list"}};
   for (auto& t : lists) {
     TIDE_CUDA(cudaMalloc((void**)t.dev, sizeof(Tile) * std::max<size_t>(1, t.host->size())),
               "cudaMalloc(tile list)");
@@ -157,33 +158,44 @@ tide_status_t check_ptr(const void* p, int64_t numel, const char* what, int64_t 
 // Copy-engine placement: per parameter one strided 2-D copy for the ranks
 // that own a full chunk (rank r's chunk is contiguous in both the buffer, at
 // r*S + o_p, and the parameter, at r*c*inner) and one plain copy for the
-// rank that owns a partial chunk.
-tide_status_t ag_copy_engine(tide_layout_s* l, const uint16_t* buf, uint16_t* const* params,
-                             cudaStream_t stream) {
+// rank that owns a partial chunk.  to_buf runs the copies backwards
+// (parameter storage -> rank-major buffer: Slot-Reuse staging).
+tide_status_t copy_engine(tide_layout_s* l, uint16_t* buf, uint16_t* const* params, bool to_buf,
+                          cudaStream_t stream) {
   const int64_t S = l->block_numel;
   for (int32_t p = 0; p < l->num_params; ++p) {
     const int64_t c = l->chunk[p], inner = l->inner[p], d0 = l->d0[p];
     if (c == 0 || inner == 0) continue;
     const int64_t full = std::min<int64_t>(l->num_ranks, d0 / c);
     const size_t width = (size_t)(c * inner) * 2;
-    const size_t spitch = (size_t)S * 2;
+    const size_t bpitch = (size_t)S * 2;
+    uint16_t* b = buf + l->offset[p];
+    uint16_t* q = params[p];
     if (full > 0) {
-      if (spitch <= (size_t)l->max_pitch && full > 1) {
-        TIDE_CUDA(cudaMemcpy2DAsync(params[p], width, buf + l->offset[p], spitch, width, (size_t)full,
-                                    cudaMemcpyDeviceToDevice, stream),
-                  "cudaMemcpy2DAsync");
+      if (bpitch <= (size_t)l->max_pitch && full > 1) {
+        cudaError_t e = to_buf ? cudaMemcpy2DAsync(b, bpitch, q, width, width, (size_t)full,
+                                                   cudaMemcpyDeviceToDevice, stream)
+                               : cudaMemcpy2DAsync(q, width, b, bpitch, width, (size_t)full,
+                                                   cudaMemcpyDeviceToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync");
       } else {
-        for (int64_t r = 0; r < full; ++r)
-          TIDE_CUDA(cudaMemcpyAsync(params[p] + r * c * inner, buf + r * S + l->offset[p], width,
-                                    cudaMemcpyDeviceToDevice, stream),
+        for (int64_t r = 0; r < full; ++r) {
+          uint16_t* x = b + r * S;
+          uint16_t* y = q + r * c * inner;
+          TIDE_CUDA(cudaMemcpyAsync(to_buf ? x : y, to_buf ? y : x, width, cudaMemcpyDeviceToDevice,
+                                    stream),
                     "cudaMemcpyAsync");
+        }
       }
     }
     const int64_t rows = d0 - full * c;
-    if (rows > 0 && full < l->num_ranks)
-      TIDE_CUDA(cudaMemcpyAsync(params[p] + full * c * inner, buf + full * S + l->offset[p],
-                                (size_t)(rows * inner) * 2, cudaMemcpyDeviceToDevice, stream),
+    if (rows > 0 && full < l->num_ranks) {
+      uint16_t* x = b + full * S;
+      uint16_t* y = q + full * c * inner;
+      TIDE_CUDA(cudaMemcpyAsync(to_buf ? x : y, to_buf ? y : x, (size_t)(rows * inner) * 2,
+                                cudaMemcpyDeviceToDevice, stream),
                 "cudaMemcpyAsync");
+    }
   }
   return TIDE_OK;
 }
@@ -203,7 +215,7 @@ namespace {
 
 // Shared steps of the kernel entry points once arguments are validated: bind
 // the device, fetch the cached device pointer table, launch.
-tide_status_t run_rs(tide_layout_s* l, int64_t t0, int64_t t1, std::vector<uintptr_t>& key,
+tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, std::vector<uintptr_t>& key,
                      const std::vector<void*>& entries, float scale, cudaStream_t stream) {
   if (t1 <= t0) return TIDE_OK;
   tide_status_t st = ensure_device(l);
@@ -213,7 +225,7 @@ tide_status_t run_rs(tide_layout_s* l, int64_t t0, int64_t t1, std::vector<uintp
   if (st != TIDE_OK) return st;
   const int64_t NP = (int64_t)l->num_ranks * l->num_params;
   RsArgs a;
-  a.tiles = l->d_rs_tiles + t0;
+  a.tiles = (staged ? l->d_st_tiles : l->d_rs_tiles) + t0;
   a.num_tiles = t1 - t0;
   a.gtab = (const uint16_t* const*)slot->d_table;
   a.stab = (float* const*)(slot->d_table + NP);
@@ -274,6 +286,7 @@ void tide_layout_destroy(tide_layout_t l) {
     cudaFree(l->d_rs_tiles);
     cudaFree(l->d_ag_tiles);
     cudaFree(l->d_pk_tiles);
+    cudaFree(l->d_st_tiles);
     if (cur >= 0 && cur != l->device) cudaSetDevice(cur);
   }
   delete l;
@@ -281,19 +294,20 @@ void tide_layout_destroy(tide_layout_t l) {
 
 tide_status_t tide_layout_launch_shape(tide_layout_t l, tide_op_t op, int32_t* grid, int32_t* block) {
   if (!l || !grid || !block) return set_error(TIDE_ERR_INVALID_ARG, "NULL argument");
-  if (op != TIDE_OP_RS && op != TIDE_OP_AG && op != TIDE_OP_PACK)
-    return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
+  if (op < TIDE_OP_RS || op > TIDE_OP_STAGED_RS) return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
   std::lock_guard<std::mutex> g(l->mu);
   DeviceShape d;
   tide_status_t st = query_device(l, &d);
   if (st != TIDE_OK) return st;
   const bool capped = l->mode == TIDE_MODE_CAPPED;
-  const int64_t tiles = op == TIDE_OP_RS   ? (int64_t)l->rs_tiles.size()
-                        : op == TIDE_OP_AG ? (int64_t)l->ag_tiles.size()
-                                           : (int64_t)l->pk_tiles.size();
-  const int occ = op == TIDE_OP_RS ? d.rs_occ : op == TIDE_OP_AG ? d.ag_occ : d.pk_occ;
+  const bool rs_like = op == TIDE_OP_RS || op == TIDE_OP_STAGED_RS;
+  const int64_t tiles = op == TIDE_OP_RS          ? (int64_t)l->rs_tiles.size()
+                        : op == TIDE_OP_STAGED_RS ? (int64_t)l->st_tiles.size()
+                        : op == TIDE_OP_PACK      ? (int64_t)l->pk_tiles.size()
+                                                  : (int64_t)l->ag_tiles.size();
+  const int occ = rs_like ? d.rs_occ : op == TIDE_OP_PACK ? d.pk_occ : d.ag_occ;
   *grid = l->mode == TIDE_MODE_COPY_ENGINE ? 0 : grid_for(tiles, l->mode, l->cta_cap, d.sms, occ);
-  *block = op == TIDE_OP_RS ? rs_block(capped) : op == TIDE_OP_AG ? ag_block(capped) : pk_block(capped);
+  *block = rs_like ? rs_block(capped) : op == TIDE_OP_PACK ? pk_block(capped) : ag_block(capped);
   return TIDE_OK;
 }
 
@@ -309,7 +323,7 @@ tide_status_t tide_rs_bf16_to_fp32(tide_layout_t l, const uint16_t* const* grads
   std::vector<void*> entries;
   tide_status_t st = rs_tables(l, -1, grads, shards, &key, &entries);
   if (st != TIDE_OK) return st;
-  return run_rs(l, 0, (int64_t)l->rs_tiles.size(), key, entries, scale, stream);
+  return run_rs(l, false, 0, (int64_t)l->rs_tiles.size(), key, entries, scale, stream);
 }
 
 tide_status_t tide_rs_bf16_to_fp32_rank(tide_layout_t l, int32_t rank, const uint16_t* const* grads,
@@ -325,7 +339,7 @@ tide_status_t tide_rs_bf16_to_fp32_rank(tide_layout_t l, int32_t rank, const uin
   std::vector<void*> entries;
   tide_status_t st = rs_tables(l, rank, grads, shards, &key, &entries);
   if (st != TIDE_OK) return st;
-  return run_rs(l, l->rs_rank_begin[rank], l->rs_rank_begin[rank + 1], key, entries, scale, stream);
+  return run_rs(l, false, l->rs_rank_begin[rank], l->rs_rank_begin[rank + 1], key, entries, scale, stream);
 }
 
 tide_status_t tide_ag_place(tide_layout_t l, const uint16_t* gathered, uint16_t* const* params,
@@ -343,7 +357,8 @@ tide_status_t tide_ag_place(tide_layout_t l, const uint16_t* gathered, uint16_t*
   if (l->ag_tiles.empty()) return TIDE_OK;
   st = ensure_device(l);
   if (st != TIDE_OK) return st;
-  if (l->mode == TIDE_MODE_COPY_ENGINE) return ag_copy_engine(l, gathered, params, stream);
+  if (l->mode == TIDE_MODE_COPY_ENGINE)
+    return copy_engine(l, const_cast<uint16_t*>(gathered), params, false, stream);
 
   std::vector<uintptr_t> key;
   key.reserve(1 + (size_t)P);
@@ -409,6 +424,76 @@ tide_status_t tide_ag_pack_bf16(tide_layout_t l, int32_t rank, const float* cons
   cudaError_t e = launch_pack(a, grid_of(l, t1 - t0, l->pk_occ), l->mode == TIDE_MODE_CAPPED, stream);
   if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
   return mark_used(l, slot, stream);
+}
+
+tide_status_t tide_rs_stage_bf16(tide_layout_t l, const uint16_t* const* grads, uint16_t* slot,
+                                 cudaStream_t stream) {
+  if (!l) return set_error(TIDE_ERR_INVALID_ARG, "layout is NULL");
+  const int32_t P = l->num_params;
+  if (P > 0 && !grads) return set_error(TIDE_ERR_INVALID_ARG, "grads table is NULL");
+  std::lock_guard<std::mutex> g(l->mu);
+  tide_status_t st = check_ptr(slot, l->block_numel * l->num_ranks, "slot", 0);
+  if (st != TIDE_OK) return st;
+  for (int32_t p = 0; p < P; ++p) {
+    st = check_ptr(grads[p], l->d0[p] * l->inner[p], "grads", p);
+    if (st != TIDE_OK) return st;
+  }
+  if (l->ag_tiles.empty()) return TIDE_OK;
+  st = ensure_device(l);
+  if (st != TIDE_OK) return st;
+  if (l->mode == TIDE_MODE_COPY_ENGINE)
+    return copy_engine(l, slot, const_cast<uint16_t* const*>(grads), true, stream);
+
+  std::vector<uintptr_t> key;
+  key.reserve(1 + (size_t)P);
+  key.push_back((uintptr_t)TIDE_OP_STAGE);
+  std::vector<void*> entries((size_t)P);
+  for (int32_t p = 0; p < P; ++p) {
+    entries[p] = (void*)grads[p];
+    key.push_back((uintptr_t)grads[p]);
+  }
+  PtrSlot* ps = nullptr;
+  st = acquire_table(l, key, entries, stream, &ps);
+  if (st != TIDE_OK) return st;
+  AgArgs a;
+  a.tiles = l->d_ag_tiles;
+  a.num_tiles = (int64_t)l->ag_tiles.size();
+  a.buf = slot;
+  a.ptab = (uint16_t* const*)ps->d_table;
+  cudaError_t e = launch_stage(a, grid_of(l, a.num_tiles, l->ag_occ), l->mode == TIDE_MODE_CAPPED, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
+  return mark_used(l, ps, stream);
+}
+
+tide_status_t tide_rs_staged_bf16_to_fp32(tide_layout_t l, const uint16_t* const* slots,
+                                          float* const* shards, float scale, cudaStream_t stream) {
+  if (!l) return set_error(TIDE_ERR_INVALID_ARG, "layout is NULL");
+  const int32_t N = l->num_ranks, P = l->num_params;
+  if (P > 0 && (!slots || !shards)) return set_error(TIDE_ERR_INVALID_ARG, "pointer table is NULL");
+  std::lock_guard<std::mutex> g(l->mu);
+  if (l->mode == TIDE_MODE_COPY_ENGINE)
+    return set_error(TIDE_ERR_UNSUPPORTED, "reduce-scatter has no copy-engine mode");
+  if (l->st_tiles.empty()) return TIDE_OK;
+  for (int32_t k = 0; k < N; ++k) {
+    tide_status_t st = check_ptr(slots[k], l->block_numel * N, "slots", k);
+    if (st != TIDE_OK) return st;
+  }
+  for (int64_t i = 0; i < (int64_t)N * P; ++i) {
+    tide_status_t st = check_ptr(shards[i], l->shard_numel[i % P], "shards", i);
+    if (st != TIDE_OK) return st;
+  }
+  // the kernel's per-parameter source table points every parameter at the
+  // slot bases; the staged tiles carry slot offsets r*S + o_p + s
+  std::vector<void*> entries((size_t)2 * N * P);
+  for (int32_t p = 0; p < P; ++p)
+    for (int32_t k = 0; k < N; ++k) entries[(size_t)p * N + k] = (void*)slots[k];
+  for (int64_t i = 0; i < (int64_t)N * P; ++i) entries[(size_t)N * P + i] = (void*)shards[i];
+  std::vector<uintptr_t> key;
+  key.reserve(2 + entries.size());
+  key.push_back((uintptr_t)TIDE_OP_STAGED_RS);
+  key.push_back(0);
+  for (void* e : entries) key.push_back((uintptr_t)e);
+  return run_rs(l, true, 0, (int64_t)l->st_tiles.size(), key, entries, scale, stream);
 }
 
 }  // extern "C"

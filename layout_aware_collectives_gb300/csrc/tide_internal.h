@@ -92,6 +92,9 @@ struct AgArgs {
 // loads in flight as one SM holds.
 cudaError_t launch_rs(const RsArgs& a, int grid, bool fat, cudaStream_t stream);
 cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, cudaStream_t stream);
+// The placement kernel run backwards (parameter storage -> rank-major
+// buffer): Slot-Reuse staging of gradients.  `buf` is written.
+cudaError_t launch_stage(const AgArgs& a, int grid, bool fat, cudaStream_t stream);
 cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, cudaStream_t stream);
 int rs_block(bool fat);
 int ag_block(bool fat);
@@ -126,7 +129,7 @@ struct tide_layout_s {
   int64_t block_numel = 0;  // S
   // RS and pack tiles are rank-major: rank r's tiles are
   // [rank_begin[r], rank_begin[r + 1]) of their list.
-  std::vector<tide::Tile> rs_tiles, ag_tiles, pk_tiles;
+  std::vector<tide::Tile> rs_tiles, ag_tiles, pk_tiles, st_tiles;
   std::vector<int64_t> rs_rank_begin, pk_rank_begin;
   tide_mode_t mode = TIDE_MODE_UNCAPPED;
   int32_t cta_cap = 0;
@@ -136,6 +139,7 @@ struct tide_layout_s {
   tide::Tile* d_rs_tiles = nullptr;
   tide::Tile* d_ag_tiles = nullptr;
   tide::Tile* d_pk_tiles = nullptr;
+  tide::Tile* d_st_tiles = nullptr;  // RS tiles whose sources are slot offsets
   int num_sms = 0;
   int rs_occ = 0, ag_occ = 0, pk_occ = 0;
   int max_pitch = 0;

@@ -55,6 +55,12 @@ class Layout:
     def pack(self, rank: int, shards, gathered, stream=None) -> None:
         _t.tide_ag_pack_bf16(self.handle, rank, shards, gathered, stream)
 
+    def stage(self, grads, slot, stream=None) -> None:
+        _t.tide_rs_stage_bf16(self.handle, grads, slot, stream)
+
+    def reduce_scatter_staged(self, slots, shards, scale: float, stream=None) -> None:
+        _t.tide_rs_staged_bf16_to_fp32(self.handle, slots, shards, scale, stream)
+
     def place(self, gathered, params, stream=None) -> None:
         _t.tide_ag_place(self.handle, gathered, params, stream)
 

@@ -35,6 +35,8 @@ TIDE_MODE_COPY_ENGINE = 2
 TIDE_OP_RS = 0
 TIDE_OP_AG = 1
 TIDE_OP_PACK = 2
+TIDE_OP_STAGE = 3
+TIDE_OP_STAGED_RS = 4
 
 TIDE_MAX_RANKS = 4096
 TIDE_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -76,6 +78,8 @@ _sig("tide_ag_place", _st, _vp, _vp, _vp, _vp)
 _sig("tide_rs_bf16_to_fp32_noalloc", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
 _sig("tide_rs_bf16_to_fp32_rank", _st, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_float, _vp)
 _sig("tide_ag_pack_bf16", _st, _vp, ctypes.c_int32, _vp, _vp, _vp)
+_sig("tide_rs_stage_bf16", _st, _vp, _vp, _vp, _vp)
+_sig("tide_rs_staged_bf16_to_fp32", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
 _sig("tide_status_string", ctypes.c_char_p, _st)
 _sig("tide_last_error", ctypes.c_char_p)
 
@@ -255,6 +259,20 @@ def tide_ag_pack_bf16(layout, rank: int, shards, gathered, stream=None) -> None:
     s = _table(shards)
     _check(_lib.tide_ag_pack_bf16(layout, rank, _tptr(s), _addr(gathered), _stream(stream)),
            "tide_ag_pack_bf16")
+
+
+def tide_rs_stage_bf16(layout, grads, slot, stream=None) -> None:
+    """grads: one rank's P bf16 gradients; slot: that rank's N*S bf16 buffer."""
+    g = _table(grads)
+    _check(_lib.tide_rs_stage_bf16(layout, _tptr(g), _addr(slot), _stream(stream)),
+           "tide_rs_stage_bf16")
+
+
+def tide_rs_staged_bf16_to_fp32(layout, slots, shards, scale: float, stream=None) -> None:
+    """slots: N staged slot buffers; shards: N*P fp32 shard pointers."""
+    a, b = _table(slots), _table(shards)
+    _check(_lib.tide_rs_staged_bf16_to_fp32(layout, _tptr(a), _tptr(b), scale, _stream(stream)),
+           "tide_rs_staged_bf16_to_fp32")
 
 
 def tide_ag_place(layout, gathered, params, stream=None) -> None:

@@ -109,6 +109,11 @@ class DeviceJob:
         self.packed = torch.full((self.N * self.S,), _i16(SENTINEL_BF16), dtype=torch.int16,
                                  device=self.device)
 
+    def make_slots(self):
+        """One N*S bf16 slot per rank (the vacated all-gather buffers), sentinel-filled."""
+        self.slots = [torch.full((self.N * self.S,), _i16(SENTINEL_BF16), dtype=torch.int16,
+                                 device=self.device) for _ in range(self.N)]
+
     def pack_src_ptrs(self, rank=None):
         if rank is None:
             return [self.pack_src[r][p] for r in range(self.N) for p in range(self.P)]

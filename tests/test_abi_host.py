@@ -259,3 +259,20 @@ def test_rank_and_pack_calls_validate_on_the_host():
         with pytest.raises(tide.TideError) as e:
             lay.reduce_scatter_rank(0, grads, mine, 0.5)
         assert e.value.status == tide.TIDE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("n,shapes,align", [
+    (4, [(256, 256), (704, 256), (256, 704), (250,)], 8),
+    (3, [(5, 3), (1,), (), (0, 4), (17, 9)], 1),
+])
+def test_staged_tiles_read_slot_offsets(n, shapes, align):
+    """Staged RS tiles write the same shard runs as the RS tiles and read
+    them at r*S + o_p + e of every slot."""
+    offs, S = oracle.layout(shapes, n, align)
+    with tide.Layout(shapes, n, align_elems=align) as lay:
+        rs = lay.tiles(tide.TIDE_OP_RS)
+        st = lay.tiles(tide.TIDE_OP_STAGED_RS)
+    assert np.array_equal(rs[:, [0, 1, 3, 4, 5]] & ~2, st[:, [0, 1, 3, 4, 5]] & ~2)
+    for p, r, src, dst, ln, flags in st:
+        if not flags & 1:
+            assert src == r * S + offs[p] + dst

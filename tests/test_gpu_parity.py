@@ -176,6 +176,53 @@ def test_ragged_rank_rs_and_pack(case, align):
         _rank_rs_and_pack(job, MODES[:2], scale=0.3)
 
 
+def _staged(job, modes, scale=None):
+    """Stage every rank's gradients into its slot, reduce-scatter from the
+    slots: slots equal the oracle's staging, shards the oracle's RS."""
+    import oracle
+
+    wl = job.wl
+    scale = wl.scale if scale is None else scale
+    offs, S = oracle.layout(wl.shapes, job.N, job.align)
+    job.make_slots()
+    for mode in modes:
+        lay = job.layout
+        lay.set_mode(*mode[1:])
+        for k in range(job.N):
+            job.slots[k].fill_(0x7FC1)
+            lay.stage([job.grads[k][p] for p in range(job.P)], job.slots[k])
+        torch.cuda.synchronize()
+        for k in range(job.N):
+            want = np.full(job.N * S, 0x7FC1, dtype=np.uint16)
+            oracle.rs_stage(wl.shapes, job.N, offs, S, [wl.host_grad(k, p) for p in range(job.P)], want)
+            assert np.array_equal(job.slots[k].cpu().numpy().view(np.uint16), want), (mode[0], k)
+        if mode[1] == tide.TIDE_MODE_COPY_ENGINE:
+            continue
+        job.reset_outputs()
+        lay.reduce_scatter_staged(job.slots, job.shard_ptrs(), scale)
+        torch.cuda.synchronize()
+        gpu_checks.full_check_rs(job, scale=scale)
+        assert job.guards_intact()
+
+
+STAGE_MODES = MODES[:3] + [("copy_engine", tide.TIDE_MODE_COPY_ENGINE, 0)]
+
+
+@pytest.mark.parametrize("mode", STAGE_MODES, ids=[m[0] for m in STAGE_MODES])
+def test_tiny_staged_rs(tiny_job, mode):
+    _staged(tiny_job, [mode])
+
+
+@pytest.mark.parametrize("align", [8, 1])
+@pytest.mark.parametrize("case", _ragged_cases(), ids=lambda c: f"N{c[0]}")
+def test_ragged_staged_rs(case, align):
+    n, shapes = case
+    wl = synth.custom(f"ragged{n}", n, shapes, sigma=0.5, seed=n)
+    with tide.Layout(wl.shapes, n, align_elems=align) as lay:
+        job = DeviceJob(wl, lay, align=align)
+        _staged(job, [MODES[0], MODES[1], STAGE_MODES[-1]], scale=0.3)
+
+
 def test_pack_special_values():
     """Ties, overflow, subnormals, infinities and NaNs through the device pack."""
     bits = np.array([0x3F800000, 0x3F808000, 0x3F818000, 0x3F808001, 0x3F807FFF, 0xBF818000,
@@ -234,6 +281,18 @@ def test_full_size_sampled_parity(name):
         torch.cuda.synchronize()
         assert gpu_checks.sampled_check_pack(job) > 0
         del job.pack_src, job.packed
+        # Slot-Reuse: stage every rank, reduce-scatter from the slots; equal
+        # bit for bit to the direct reduce-scatter
+        ref_all = [[s.clone() for s in row] for row in job.shards]
+        job.make_slots()
+        for k in range(job.N):
+            lay.stage([job.grads[k][p] for p in range(job.P)], job.slots[k])
+        lay.reduce_scatter_staged(job.slots, job.shard_ptrs(), wl.scale)
+        torch.cuda.synchronize()
+        for r in range(job.N):
+            for p in range(job.P):
+                assert torch.equal(job.shards[r][p].view(torch.int32), ref_all[r][p].view(torch.int32))
+        del job.slots, ref_all
         ref = [s.clone() for s in (job.shards[0][0], job.shards[-1][-1])]
         lay.set_mode(tide.TIDE_MODE_CAPPED, 64)
         for row in job.shards:

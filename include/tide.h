@@ -36,9 +36,12 @@
  * alignment in elements (8 by default: every shard starts on 16 bytes).
  *
  * Conventions for every call:
- *  - All device pointers are CUDA device pointers of the device that is
- *    current when the layout is first used; tables of pointers are HOST
- *    arrays read only during the call.  The caller owns every device buffer
+ *  - All device pointers are addresses the device that is current when the
+ *    layout is first used can load from / store to: device memory, or pinned
+ *    host memory mapped into the device address space (on Grace systems the
+ *    kernels then read inputs and write results over NVLink-C2C with no
+ *    separate copy).  Tables of pointers are HOST arrays read only during
+ *    the call.  The caller owns every device buffer
  *    and keeps it alive until the work enqueued on `stream` completes.
  *  - Compute calls are asynchronous with respect to the host and never
  *    synchronise the device.  The first compute call of a layout uploads its

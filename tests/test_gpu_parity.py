@@ -316,3 +316,27 @@ def test_int64_offsets():
         assert gpu_checks.sampled_check_ag(job, per=64) > 0
         del job
         torch.cuda.empty_cache()
+
+
+def test_zero_copy_host_buffers(tiny_job):
+    """Inputs and outputs in pinned host memory, read and written by the
+    kernels directly: same bits as the oracle."""
+    import bench
+
+    job = tiny_job
+    h_g = [[g.cpu().pin_memory() for g in row] for row in job.grads]
+    h_buf = job.gathered.cpu().pin_memory()
+    h_s = [[torch.full_like(s.cpu(), float("nan")).pin_memory() for s in row] for row in job.shards]
+    h_p = [torch.zeros_like(p.cpu()).pin_memory() for p in job.params]
+    flat = [t for row in h_g for t in row] + [t for row in h_s for t in row] + h_p + [h_buf]
+    if not bench._host_mapped(flat):
+        pytest.skip("pinned host memory is not device-mapped here")
+    job.layout.reduce_scatter([t for row in h_g for t in row], [t for row in h_s for t in row],
+                              job.wl.scale)
+    job.layout.place(h_buf, h_p)
+    torch.cuda.synchronize()
+    job.shards = h_s
+    job.params = h_p
+    job.gathered = h_buf
+    gpu_checks.full_check_rs(job)
+    gpu_checks.full_check_ag(job)

@@ -757,6 +757,8 @@ def run_interference(tide, layout, job, wl, props):
     modes = [("rs", "uncapped", tide.TIDE_MODE_UNCAPPED, 0)]
     modes += [("rs", f"capped{cap}", tide.TIDE_MODE_CAPPED, cap) for cap in (8, 16, 32, 64)]
     modes += [("ag", "uncapped", tide.TIDE_MODE_UNCAPPED, 0),
+              ("ag", "bulk_tma", tide.TIDE_MODE_BULK, 0),
+              ("ag", "capped16", tide.TIDE_MODE_CAPPED, 16),
               ("ag", "copy_engine", tide.TIDE_MODE_COPY_ENGINE, 0)]
     for kind, name, mode, cap in modes:
         layout.set_mode(mode, cap)

@@ -95,7 +95,13 @@ typedef enum {
   /* Placement through the copy engines (cudaMemcpy2DAsync, no SM use), the
    * copy-engine path of "TIDE的设计思路".  Reduce-scatter has no copy-engine
    * form: it returns TIDE_ERR_UNSUPPORTED in this mode. */
-  TIDE_MODE_COPY_ENGINE = 2
+  TIDE_MODE_COPY_ENGINE = 2,
+  /* Placement and staging through the TMA bulk-copy engine (cp.async.bulk
+   * global -> shared -> global, one issuing lane per CTA, 64 KiB ring, every
+   * wait bounded; see tide_layout_check_device); the reduce-scatter and the
+   * pack run as in TIDE_MODE_UNCAPPED.  Measured ~2% below the load/store
+   * kernel on GB300, kept for comparison. */
+  TIDE_MODE_BULK = 3
 } tide_mode_t;
 
 /* Operations, for the launch-shape and tile-list queries. */
@@ -309,6 +315,24 @@ TIDE_API tide_status_t tide_rs_staged_bf16_to_fp32(tide_layout_t layout, const u
 TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t layout, const uint16_t* const* grads,
                                                     float* const* shards, float scale,
                                                     cudaStream_t stream);
+
+/*
+ * Device-side failure report.  Synchronises the device, then reads and clears
+ * the layout's device error word: TIDE_ERR_TIMEOUT if, since the last check,
+ * a bounded wait inside a bulk-copy (TMA engine) kernel of this layout ran
+ * out — the kernel then abandoned its remaining copies, so the outputs of
+ * that call are incomplete — else TIDE_OK.  The wait bound is 2 s.
+ */
+TIDE_API tide_status_t tide_layout_check_device(tide_layout_t layout);
+
+/*
+ * Test hook for the bounded waits: with ns > 0, every following bulk-copy
+ * launch of this layout waits on a barrier nothing arrives on, bounded by ns
+ * nanoseconds, reports the timeout through the error word and copies
+ * nothing; ns = 0 turns the hook off.  Lets tests exercise the timeout path
+ * without faulting or hanging a GPU.
+ */
+TIDE_API tide_status_t tide_layout_set_test_stall(tide_layout_t layout, int64_t ns);
 
 /* Static description of a status code. */
 TIDE_API const char* tide_status_string(tide_status_t status);

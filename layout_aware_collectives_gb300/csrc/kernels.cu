@@ -205,6 +205,190 @@ __global__ void __launch_bounds__(THREADS) ag_kernel(AgArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- bulk-copy placement
+// The same segmented copy driven by the TMA engine: one lane per CTA issues
+// cp.async.bulk global->shared copies of TIDE_BULK_CHUNK bytes into a ring of
+// stages (completion tracked by one mbarrier per stage) and
+// cp.async.bulk shared->global copies out of them, so the SM's load/store
+// units carry almost nothing.  Only 16-byte-aligned vector runs go through
+// the bulk path (their addresses and sizes are multiples of 16 bytes by
+// construction); the rest of the warp copies unaligned runs and the < 8
+// element tails with plain loads.  Every mbarrier wait is bounded by
+// %globaltimer: on timeout the kernel sets *err, waits (bounded) for its own
+// copies in flight and returns.
+namespace bulk {
+
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(saddr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// True once the phase with `parity` has completed; false after timeout_ns.
+__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = now_ns();
+  while (!mbar_test(bar, parity)) {
+    if (now_ns() - t0 > timeout_ns) return false;
+    __nanosleep(32);
+  }
+  return true;
+}
+
+// L2 policy for data touched once: evict first (as the streaming loads and
+// stores of the load/store kernels).
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void g2s(void* smem, const void* gmem, uint32_t bytes, uint64_t* bar,
+                                    uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, "
+      "[%3], %4;" ::"r"(saddr(smem)),
+      "l"(gmem), "r"(bytes), "r"(saddr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void s2g(void* gmem, const void* smem, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gmem),
+               "r"(saddr(smem)), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// All but the `n` most recent bulk groups have finished reading shared memory.
+template <int n>
+__device__ __forceinline__ void wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(n) : "memory");
+}
+
+__device__ __forceinline__ void wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Walks this CTA's vector runs (tiles blockIdx.x, +gridDim.x, ...) in
+// chunks of at most TIDE_BULK_CHUNK bytes.
+struct Cursor {
+  int64_t t;
+  const unsigned char* src;
+  unsigned char* dst;
+  uint64_t bytes, off;
+};
+
+template <bool TO_BUF>
+__device__ __forceinline__ bool next_chunk(Cursor& c, const AgArgs& a, const void*& src, void*& dst,
+                                           uint32_t& n) {
+  while (c.off >= c.bytes) {
+    c.t += gridDim.x;
+    if (c.t >= a.num_tiles) return false;
+    const Tile tile = a.tiles[c.t];
+    c.off = 0;
+    c.bytes = (tile.flags & kTileVec) ? (uint64_t)(tile.len & ~7) * 2u : 0u;
+    const unsigned char* b = (const unsigned char*)(a.buf + tile.src);
+    const unsigned char* q = (const unsigned char*)(a.ptab[tile.p] + tile.dst);
+    c.src = TO_BUF ? q : b;
+    c.dst = (unsigned char*)(TO_BUF ? b : q);
+  }
+  const uint64_t left = c.bytes - c.off;
+  n = left < (uint64_t)TIDE_BULK_CHUNK ? (uint32_t)left : (uint32_t)TIDE_BULK_CHUNK;
+  src = c.src + c.off;
+  dst = c.dst + c.off;
+  c.off += n;
+  return true;
+}
+
+}  // namespace bulk
+
+template <bool TO_BUF>
+__global__ void __launch_bounds__(32) ag_bulk_kernel(AgArgs a) {
+  constexpr int S = TIDE_BULK_STAGES;
+  extern __shared__ __align__(128) unsigned char bulk_smem[];
+  unsigned char(*stage)[TIDE_BULK_CHUNK] = (unsigned char(*)[TIDE_BULK_CHUNK])bulk_smem;
+  uint64_t* full = (uint64_t*)(bulk_smem + (size_t)S * TIDE_BULK_CHUNK);  // S + 1; [S]: test hook
+
+  // plain-copy parts: unaligned runs, and the < 8 element tails of vector runs
+  for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+    const Tile tile = a.tiles[t];
+    const uint16_t* b = a.buf + tile.src;
+    uint16_t* q = a.ptab[tile.p] + tile.dst;
+    const uint16_t* src = TO_BUF ? q : b;
+    uint16_t* dst = TO_BUF ? const_cast<uint16_t*>(b) : q;
+    for (int e = ((tile.flags & kTileVec) ? (tile.len & ~7) : 0) + threadIdx.x; e < tile.len; e += 32)
+      dst[e] = ld_stream_u16(src + e);
+  }
+  if (threadIdx.x != 0) return;
+
+  for (int s = 0; s <= S; ++s) bulk::mbar_init(&full[s], 1);
+  bulk::fence_mbar_init();
+  if (a.test_stall_ns) {  // a barrier nothing arrives on: the wait must run out
+    if (!bulk::mbar_wait(&full[S], 0, a.test_stall_ns)) atomicExch(a.err, kDevErrTimeout);
+    return;
+  }
+
+  const uint64_t pol = bulk::evict_first_policy();
+  bulk::Cursor lc{(int64_t)blockIdx.x - (int64_t)gridDim.x, nullptr, nullptr, 0, 0};
+  bulk::Cursor sc = lc;
+  const void* src;
+  void* dst;
+  uint32_t n;
+  int64_t issued = 0;
+  for (; issued < S - 1 && bulk::next_chunk<TO_BUF>(lc, a, src, dst, n); ++issued) {
+    bulk::mbar_expect_tx(&full[issued % S], n);
+    bulk::g2s(stage[issued % S], src, n, &full[issued % S], pol);
+  }
+  for (int64_t j = 0; j < issued; ++j) {
+    const int s = (int)(j % S);
+    if (!bulk::mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.timeout_ns)) {
+      atomicExch(a.err, kDevErrTimeout);
+      for (int64_t k = j; k < issued; ++k)  // loads that may still land in this CTA's shared memory
+        bulk::mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), a.timeout_ns);
+      bulk::wait_all();
+      return;
+    }
+    bulk::next_chunk<TO_BUF>(sc, a, src, dst, n);
+    bulk::s2g(dst, stage[s], n, pol);
+    bulk::commit();
+    // chunk `issued` goes to stage (j - 1) % S, last read by the store of
+    // chunk j - 1: wait until only the store just issued may still read
+    if (bulk::next_chunk<TO_BUF>(lc, a, src, dst, n)) {
+      bulk::wait_read<1>();
+      const int s2 = (int)(issued % S);
+      bulk::mbar_expect_tx(&full[s2], n);
+      bulk::g2s(stage[s2], src, n, &full[s2], pol);
+      ++issued;
+    }
+  }
+  bulk::wait_all();
+}
+
 // ---------------------------------------------------------------- all-gather input pack
 // fp32 -> bf16 bits, round to nearest with ties to even on the 16 dropped
 // bits (the usual add-half-ulp-plus-lowest-kept-bit method); a NaN keeps its
@@ -315,6 +499,24 @@ cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, cudaStream_t stre
   else
     pack_kernel<kAgThreads><<<grid, kAgThreads, 0, stream>>>(a);
   return cudaGetLastError();
+}
+
+constexpr size_t kBulkSmem = (size_t)TIDE_BULK_STAGES * TIDE_BULK_CHUNK + 8 * (TIDE_BULK_STAGES + 1);
+
+cudaError_t launch_ag_bulk(const AgArgs& a, int grid, bool to_buf, cudaStream_t stream) {
+  if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
+  auto k = to_buf ? ag_bulk_kernel<true> : ag_bulk_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, 32, kBulkSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t ag_bulk_occupancy(int* blocks_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(ag_bulk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kBulkSmem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, ag_bulk_kernel<false>, 32, kBulkSmem);
 }
 
 cudaError_t pk_occupancy(int* blocks_per_sm) {

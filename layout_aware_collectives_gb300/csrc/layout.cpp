@@ -256,7 +256,8 @@ tide_status_t tide_layout_valid_rows(tide_layout_t l, int32_t p, int32_t r, int6
 
 tide_status_t tide_layout_set_mode(tide_layout_t l, tide_mode_t mode, int32_t cta_cap) {
   if (!l) return set_error(TIDE_ERR_INVALID_ARG, "NULL layout");
-  if (mode != TIDE_MODE_UNCAPPED && mode != TIDE_MODE_CAPPED && mode != TIDE_MODE_COPY_ENGINE)
+  if (mode != TIDE_MODE_UNCAPPED && mode != TIDE_MODE_CAPPED && mode != TIDE_MODE_COPY_ENGINE &&
+      mode != TIDE_MODE_BULK)
     return set_error(TIDE_ERR_INVALID_ARG, "unknown mode");
   if (mode == TIDE_MODE_CAPPED && cta_cap < 1)
     return set_error(TIDE_ERR_INVALID_ARG, "cta_cap must be >= 1 in TIDE_MODE_CAPPED");

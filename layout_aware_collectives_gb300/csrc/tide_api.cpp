@@ -18,7 +18,7 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
   } while (0)
 
 struct DeviceShape {
-  int sms = 0, rs_occ = 0, ag_occ = 0, pk_occ = 0;
+  int sms = 0, rs_occ = 0, ag_occ = 0, pk_occ = 0, bulk_occ = 0;
 };
 
 tide_status_t query_device(const tide_layout_s* l, DeviceShape* d) {
@@ -29,9 +29,11 @@ tide_status_t query_device(const tide_layout_s* l, DeviceShape* d) {
   TIDE_CUDA(rs_occupancy(l->num_ranks, &d->rs_occ), "occupancy of the reduce-scatter kernel");
   TIDE_CUDA(ag_occupancy(&d->ag_occ), "occupancy of the placement kernel");
   TIDE_CUDA(pk_occupancy(&d->pk_occ), "occupancy of the pack kernel");
+  TIDE_CUDA(ag_bulk_occupancy(&d->bulk_occ), "occupancy of the bulk-copy kernel");
   d->rs_occ = std::max(1, d->rs_occ);
   d->ag_occ = std::max(1, d->ag_occ);
   d->pk_occ = std::max(1, d->pk_occ);
+  d->bulk_occ = std::max(1, d->bulk_occ);
   return TIDE_OK;
 }
 
@@ -73,6 +75,8 @@ tide_status_t ensure_device(tide_layout_s* l) {
                            cudaMemcpyHostToDevice),
                 t.what);
   }
+  TIDE_CUDA(cudaMalloc((void**)&l->d_err, sizeof(int)), "cudaMalloc(error word)");
+  TIDE_CUDA(cudaMemset(l->d_err, 0, sizeof(int)), "cudaMemset(error word)");
   for (PtrSlot& s : l->slots) {
     TIDE_CUDA(cudaEventCreateWithFlags(&s.upload_ev, cudaEventDisableTiming), "cudaEventCreate");
     TIDE_CUDA(cudaEventCreateWithFlags(&s.use_ev, cudaEventDisableTiming), "cudaEventCreate");
@@ -81,6 +85,7 @@ tide_status_t ensure_device(tide_layout_s* l) {
   l->rs_occ = d.rs_occ;
   l->ag_occ = d.ag_occ;
   l->pk_occ = d.pk_occ;
+  l->bulk_occ = d.bulk_occ;
   l->device = dev;
   return TIDE_OK;
 }
@@ -265,6 +270,19 @@ tide_status_t rs_tables(tide_layout_s* l, int32_t rank, const uint16_t* const* g
   return TIDE_OK;
 }
 
+// Placement (to_buf = false) or staging (to_buf = true) over the AG tile
+// list: the bulk-copy kernel in TIDE_MODE_BULK, else the load/store kernel.
+cudaError_t launch_copy(tide_layout_s* l, AgArgs& a, bool to_buf, cudaStream_t stream) {
+  a.err = l->d_err;
+  a.timeout_ns = TIDE_BULK_TIMEOUT_NS;
+  a.test_stall_ns = (uint64_t)l->test_stall_ns;
+  const bool capped = l->mode == TIDE_MODE_CAPPED;
+  if (l->mode == TIDE_MODE_BULK)
+    return launch_ag_bulk(a, grid_of(l, a.num_tiles, l->bulk_occ), to_buf, stream);
+  return to_buf ? launch_stage(a, grid_of(l, a.num_tiles, l->ag_occ), capped, stream)
+                : launch_ag(a, grid_of(l, a.num_tiles, l->ag_occ), capped, stream);
+}
+
 }  // namespace
 }  // namespace tide
 
@@ -287,6 +305,7 @@ void tide_layout_destroy(tide_layout_t l) {
     cudaFree(l->d_ag_tiles);
     cudaFree(l->d_pk_tiles);
     cudaFree(l->d_st_tiles);
+    cudaFree(l->d_err);
     if (cur >= 0 && cur != l->device) cudaSetDevice(cur);
   }
   delete l;
@@ -305,9 +324,10 @@ tide_status_t tide_layout_launch_shape(tide_layout_t l, tide_op_t op, int32_t* g
                         : op == TIDE_OP_STAGED_RS ? (int64_t)l->st_tiles.size()
                         : op == TIDE_OP_PACK      ? (int64_t)l->pk_tiles.size()
                                                   : (int64_t)l->ag_tiles.size();
-  const int occ = rs_like ? d.rs_occ : op == TIDE_OP_PACK ? d.pk_occ : d.ag_occ;
+  const bool bulk = l->mode == TIDE_MODE_BULK && (op == TIDE_OP_AG || op == TIDE_OP_STAGE);
+  const int occ = rs_like ? d.rs_occ : op == TIDE_OP_PACK ? d.pk_occ : bulk ? d.bulk_occ : d.ag_occ;
   *grid = l->mode == TIDE_MODE_COPY_ENGINE ? 0 : grid_for(tiles, l->mode, l->cta_cap, d.sms, occ);
-  *block = rs_like ? rs_block(capped) : op == TIDE_OP_PACK ? pk_block(capped) : ag_block(capped);
+  *block = rs_like ? rs_block(capped) : op == TIDE_OP_PACK ? pk_block(capped) : bulk ? 32 : ag_block(capped);
   return TIDE_OK;
 }
 
@@ -377,7 +397,7 @@ tide_status_t tide_ag_place(tide_layout_t l, const uint16_t* gathered, uint16_t*
   a.num_tiles = (int64_t)l->ag_tiles.size();
   a.buf = gathered;
   a.ptab = (uint16_t* const*)slot->d_table;
-  cudaError_t e = launch_ag(a, grid_of(l, a.num_tiles, l->ag_occ), l->mode == TIDE_MODE_CAPPED, stream);
+  cudaError_t e = launch_copy(l, a, false, stream);
   if (e != cudaSuccess) return cuda_fail(e, "placement kernel launch");
   return mark_used(l, slot, stream);
 }
@@ -460,7 +480,7 @@ tide_status_t tide_rs_stage_bf16(tide_layout_t l, const uint16_t* const* grads, 
   a.num_tiles = (int64_t)l->ag_tiles.size();
   a.buf = slot;
   a.ptab = (uint16_t* const*)ps->d_table;
-  cudaError_t e = launch_stage(a, grid_of(l, a.num_tiles, l->ag_occ), l->mode == TIDE_MODE_CAPPED, stream);
+  cudaError_t e = launch_copy(l, a, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
   return mark_used(l, ps, stream);
 }
@@ -494,6 +514,25 @@ tide_status_t tide_rs_staged_bf16_to_fp32(tide_layout_t l, const uint16_t* const
   key.push_back(0);
   for (void* e : entries) key.push_back((uintptr_t)e);
   return run_rs(l, true, 0, (int64_t)l->st_tiles.size(), key, entries, scale, stream);
+}
+
+tide_status_t tide_layout_check_device(tide_layout_t l) {
+  if (!l) return set_error(TIDE_ERR_INVALID_ARG, "layout is NULL");
+  std::lock_guard<std::mutex> g(l->mu);
+  if (l->device < 0) return TIDE_OK;  // nothing launched yet
+  TIDE_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  int v = 0;
+  TIDE_CUDA(cudaMemcpy(&v, l->d_err, sizeof v, cudaMemcpyDeviceToHost), "read of the error word");
+  if (v == 0) return TIDE_OK;
+  TIDE_CUDA(cudaMemset(l->d_err, 0, sizeof(int)), "reset of the error word");
+  return set_error(TIDE_ERR_TIMEOUT, "a bounded wait in a bulk-copy kernel ran out; its copies were abandoned");
+}
+
+tide_status_t tide_layout_set_test_stall(tide_layout_t l, int64_t ns) {
+  if (!l || ns < 0) return set_error(TIDE_ERR_INVALID_ARG, "NULL layout or negative time");
+  std::lock_guard<std::mutex> g(l->mu);
+  l->test_stall_ns = ns;
+  return TIDE_OK;
 }
 
 }  // extern "C"

@@ -84,7 +84,24 @@ struct AgArgs {
   int64_t num_tiles;
   const uint16_t* buf;
   uint16_t* const* ptab;
+  // bulk-copy kernel only: error word set when a bounded wait runs out,
+  // the bound, and a test hook that makes the first wait run out
+  int* err;
+  uint64_t timeout_ns;
+  uint64_t test_stall_ns;
 };
+
+#ifndef TIDE_BULK_STAGES
+#define TIDE_BULK_STAGES 4
+#endif
+#ifndef TIDE_BULK_CHUNK  // bytes per bulk copy (multiple of 16)
+#define TIDE_BULK_CHUNK 16384
+#endif
+#ifndef TIDE_BULK_TIMEOUT_NS  // bound of every mbarrier wait of the bulk kernel
+#define TIDE_BULK_TIMEOUT_NS 2000000000ull
+#endif
+// Error codes written to the device error word.
+constexpr int kDevErrTimeout = 1;
 
 // Kernel launchers (kernels.cu).  Return the launch's cudaError_t.  `fat`
 // selects the kFatThreads-wide CTA used by the CTA-capped mode: a capped CTA
@@ -95,6 +112,10 @@ cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, cudaStream_t stream);
 // The placement kernel run backwards (parameter storage -> rank-major
 // buffer): Slot-Reuse staging of gradients.  `buf` is written.
 cudaError_t launch_stage(const AgArgs& a, int grid, bool fat, cudaStream_t stream);
+// Bulk-copy (TMA engine) placement / staging: one issuing lane per CTA,
+// shared-memory ring of TIDE_BULK_STAGES x TIDE_BULK_CHUNK bytes.
+cudaError_t launch_ag_bulk(const AgArgs& a, int grid, bool to_buf, cudaStream_t stream);
+cudaError_t ag_bulk_occupancy(int* blocks_per_sm);
 cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, cudaStream_t stream);
 int rs_block(bool fat);
 int ag_block(bool fat);
@@ -141,7 +162,9 @@ struct tide_layout_s {
   tide::Tile* d_pk_tiles = nullptr;
   tide::Tile* d_st_tiles = nullptr;  // RS tiles whose sources are slot offsets
   int num_sms = 0;
-  int rs_occ = 0, ag_occ = 0, pk_occ = 0;
+  int rs_occ = 0, ag_occ = 0, pk_occ = 0, bulk_occ = 0;
+  int* d_err = nullptr;         // device error word of the bulk-copy kernels
+  int64_t test_stall_ns = 0;    // test hook of the bounded waits
   int max_pitch = 0;
   tide::PtrSlot slots[tide::kPtrSlots];
   uint64_t use_counter = 0;

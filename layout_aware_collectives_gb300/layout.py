@@ -45,6 +45,12 @@ class Layout:
     def set_mode(self, mode: int, cta_cap: int = 0) -> None:
         _t.tide_layout_set_mode(self.handle, mode, cta_cap)
 
+    def check_device(self) -> None:
+        _t.tide_layout_check_device(self.handle)
+
+    def set_test_stall(self, ns: int) -> None:
+        _t.tide_layout_set_test_stall(self.handle, ns)
+
     # -------- compute
     def reduce_scatter(self, grads, shards, scale: float, stream=None) -> None:
         _t.tide_rs_bf16_to_fp32(self.handle, grads, shards, scale, stream)

@@ -31,6 +31,7 @@ TIDE_ERR_OUT_OF_MEMORY = 6
 TIDE_MODE_UNCAPPED = 0
 TIDE_MODE_CAPPED = 1
 TIDE_MODE_COPY_ENGINE = 2
+TIDE_MODE_BULK = 3
 
 TIDE_OP_RS = 0
 TIDE_OP_AG = 1
@@ -80,6 +81,8 @@ _sig("tide_rs_bf16_to_fp32_rank", _st, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_f
 _sig("tide_ag_pack_bf16", _st, _vp, ctypes.c_int32, _vp, _vp, _vp)
 _sig("tide_rs_stage_bf16", _st, _vp, _vp, _vp, _vp)
 _sig("tide_rs_staged_bf16_to_fp32", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
+_sig("tide_layout_check_device", _st, _vp)
+_sig("tide_layout_set_test_stall", _st, _vp, ctypes.c_int64)
 _sig("tide_status_string", ctypes.c_char_p, _st)
 _sig("tide_last_error", ctypes.c_char_p)
 
@@ -136,6 +139,15 @@ def _table(x) -> PointerTable | None:
 
 def _tptr(t: PointerTable | None) -> int:
     return t.ptr if t is not None and t.n else 0
+
+
+def tide_layout_check_device(layout) -> None:
+    """Raises TideError(TIDE_ERR_TIMEOUT) if a bounded device wait ran out."""
+    _check(_lib.tide_layout_check_device(layout), "tide_layout_check_device")
+
+
+def tide_layout_set_test_stall(layout, ns: int) -> None:
+    _check(_lib.tide_layout_set_test_stall(layout, ns), "tide_layout_set_test_stall")
 
 
 def tide_status_string(status: int) -> str:

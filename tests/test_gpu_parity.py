@@ -22,7 +22,8 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU-only ho
 import layout_aware_collectives_gb300 as tide  # noqa: E402
 
 MODES = [("uncapped", tide.TIDE_MODE_UNCAPPED, 0)] + [
-    (f"capped{c}", tide.TIDE_MODE_CAPPED, c) for c in (1, 2, 7, 8, 32)]
+    (f"capped{c}", tide.TIDE_MODE_CAPPED, c) for c in (1, 2, 7, 8, 32)] + [
+    ("bulk", tide.TIDE_MODE_BULK, 0)]
 
 
 def run(job, rs_mode=None, ag_mode=None, scale=None):
@@ -127,7 +128,7 @@ def test_ragged_shapes_full_parity(case, align):
     with tide.Layout(wl.shapes, n, align_elems=align) as lay:
         job = DeviceJob(wl, lay, align=align)
         gpu_checks.check_layout(job)
-        for mode in MODES[:3]:
+        for mode in MODES[:3] + MODES[-1:]:
             job.reset_outputs()
             run(job, rs_mode=mode[1:], ag_mode=mode[1:], scale=0.3)
             gpu_checks.full_check_rs(job, scale=0.3)
@@ -205,7 +206,8 @@ def _staged(job, modes, scale=None):
         assert job.guards_intact()
 
 
-STAGE_MODES = MODES[:3] + [("copy_engine", tide.TIDE_MODE_COPY_ENGINE, 0)]
+STAGE_MODES = MODES[:3] + [("bulk", tide.TIDE_MODE_BULK, 0),
+                           ("copy_engine", tide.TIDE_MODE_COPY_ENGINE, 0)]
 
 
 @pytest.mark.parametrize("mode", STAGE_MODES, ids=[m[0] for m in STAGE_MODES])
@@ -220,7 +222,7 @@ def test_ragged_staged_rs(case, align):
     wl = synth.custom(f"ragged{n}", n, shapes, sigma=0.5, seed=n)
     with tide.Layout(wl.shapes, n, align_elems=align) as lay:
         job = DeviceJob(wl, lay, align=align)
-        _staged(job, [MODES[0], MODES[1], STAGE_MODES[-1]], scale=0.3)
+        _staged(job, [MODES[0], MODES[1], STAGE_MODES[-2], STAGE_MODES[-1]], scale=0.3)
 
 
 def test_pack_special_values():
@@ -339,4 +341,26 @@ def test_zero_copy_host_buffers(tiny_job):
     job.params = h_p
     job.gathered = h_buf
     gpu_checks.full_check_rs(job)
+    gpu_checks.full_check_ag(job)
+
+
+def test_bounded_wait_timeout_is_reported(tiny_job):
+    """The bulk-copy kernel's waits are bounded: with the test hook set, its
+    wait on a barrier nothing arrives on runs out after 1 ms, the kernel
+    returns, and the host reads TIDE_ERR_TIMEOUT; the next call (hook off)
+    completes and matches the oracle."""
+    job = tiny_job
+    lay = job.layout
+    lay.set_mode(tide.TIDE_MODE_BULK)
+    assert lay.launch_shape(tide.TIDE_OP_AG)[1] == 32
+    lay.set_test_stall(1_000_000)
+    lay.place(job.gathered, job.param_ptrs())
+    with pytest.raises(tide.TideError) as e:
+        lay.check_device()
+    assert e.value.status == tide.TIDE_ERR_TIMEOUT
+    lay.check_device()  # cleared
+    lay.set_test_stall(0)
+    job.reset_outputs()
+    lay.place(job.gathered, job.param_ptrs())
+    lay.check_device()
     gpu_checks.full_check_ag(job)

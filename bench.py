@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stock", action="store_true")
+    ap.add_argument("--mode", default="uncapped", choices=["uncapped", "capped", "bulk"],
+                    help="kernel mode of the timed step")
+    ap.add_argument("--cap", type=int, default=0, help="CTA cap for --mode capped / bulk")
     return ap.parse_args()
 
 
@@ -336,6 +339,12 @@ def run_tide(args):
     small = (rs_bytes + ag_bytes) < 2 * L2_BYTES
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if small else None
 
+    step_mode = {"uncapped": tide.TIDE_MODE_UNCAPPED, "capped": tide.TIDE_MODE_CAPPED,
+                 "bulk": tide.TIDE_MODE_BULK}[args.mode]
+    if args.mode == "capped" and args.cap < 1:
+        raise SystemExit("--mode capped needs --cap >= 1")
+    layout.set_mode(step_mode, args.cap)
+
     def step():
         layout.reduce_scatter(gptr, sptr, scale, stream)
         layout.place(job.gathered, pptr, stream)
@@ -390,23 +399,28 @@ def run_tide(args):
                    "psi": wl.psi, "rs_bytes": rs_bytes, "ag_bytes": ag_bytes,
                    "l2": "flushed between steps" if small else
                    f"inputs larger than L2 ({(rs_bytes + ag_bytes) / 1e9:.1f} GB per step)",
-                   "mode": "uncapped", "parallelism": f"replicas x{world}"},
+                   "mode": args.mode + (f" cap {args.cap}" if args.cap else ""),
+                   "parallelism": f"replicas x{world}"},
         "kernels": {
             "rs": {"ms": round(rs_avg, 4), "GB/s": round(rs_gbs, 1), "frac": round(rs_gbs / peak, 4),
                    "grid": grid_rs, "block": block_rs},
             "ag": {"ms": round(ag_avg, 4), "GB/s": round(ag_gbs, 1), "frac": round(ag_gbs / peak, 4),
                    "grid": grid_ag, "block": block_ag},
         },
-        "roofline": {"bound": "hbm", "kernel": "tide rs_kernel", "achieved": round(rs_gbs, 1),
+        "roofline": {"bound": "hbm",
+                     "kernel": "tide rs_bulk_kernel" if args.mode == "bulk" else "tide rs_kernel",
+                     "achieved": round(rs_gbs, 1),
                      "peak": peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(rs_gbs / peak, 4),
-                     "traffic": recorded_traffic(wl.name)},
+                     "traffic": recorded_traffic(wl.name) if args.mode == "uncapped" else None},
         "clocks": clk,
         "gpu_launches": 2 * K,
         "device": props.name,
     }
 
+    layout.check_device()  # raises if a bounded device wait ran out during the timed steps
+    layout.set_mode(tide.TIDE_MODE_UNCAPPED)
     out["next_ops"] = run_next_ops(tide, layout, job, wl, stream)
     if not args.no_stock:
         out["stock_fsdp2"] = run_stock(job, wl, stream, rs_avg, ag_avg)
@@ -756,6 +770,8 @@ def run_interference(tide, layout, job, wl, props):
            "gemm_tflops_alone": round(flops / (t0 * 1e-3) / 1e12, 1), "modes": []}
     modes = [("rs", "uncapped", tide.TIDE_MODE_UNCAPPED, 0)]
     modes += [("rs", f"capped{cap}", tide.TIDE_MODE_CAPPED, cap) for cap in (8, 16, 32, 64)]
+    modes += [("rs", f"bulk_tma_capped{cap}", tide.TIDE_MODE_BULK, cap) for cap in (8, 16, 32, 64)]
+    modes += [("rs", "bulk_tma_uncapped", tide.TIDE_MODE_BULK, 0)]
     modes += [("ag", "uncapped", tide.TIDE_MODE_UNCAPPED, 0),
               ("ag", "bulk_tma", tide.TIDE_MODE_BULK, 0),
               ("ag", "capped16", tide.TIDE_MODE_CAPPED, 16),

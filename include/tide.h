@@ -96,11 +96,15 @@ typedef enum {
    * copy-engine path of "TIDE的设计思路".  Reduce-scatter has no copy-engine
    * form: it returns TIDE_ERR_UNSUPPORTED in this mode. */
   TIDE_MODE_COPY_ENGINE = 2,
-  /* Placement and staging through the TMA bulk-copy engine (cp.async.bulk
-   * global -> shared -> global, one issuing lane per CTA, 64 KiB ring, every
-   * wait bounded; see tide_layout_check_device); the reduce-scatter and the
-   * pack run as in TIDE_MODE_UNCAPPED.  Measured ~2% below the load/store
-   * kernel on GB300, kept for comparison. */
+  /* The TMA bulk-copy engine (cp.async.bulk, mbarriers, every wait bounded;
+   * see tide_layout_check_device).  Placement and staging: global -> shared
+   * -> global copies issued by one lane per CTA.  Reduce-scatter (all three
+   * forms, N <= 512; larger N runs the load/store kernel): one 288-thread
+   * CTA per SM whose producer warp stages the N rank slices of each chunk
+   * (32 KiB per chunk, 64 KiB when capped) in a 192 KiB shared-memory ring
+   * and whose 8 consumer warps sum them.  The pack runs as in
+   * TIDE_MODE_UNCAPPED.  cta_cap > 0 caps the grid at cta_cap CTAs (one per
+   * SM), cta_cap = 0 uses every SM. */
   TIDE_MODE_BULK = 3
 } tide_mode_t;
 
@@ -161,7 +165,7 @@ TIDE_API tide_status_t tide_layout_valid_rows(tide_layout_t layout, int32_t p, i
 TIDE_API tide_status_t tide_layout_chunk_rows(tide_layout_t layout, int32_t p, int64_t* rows);
 
 /* Select how the compute calls run (default TIDE_MODE_UNCAPPED).  cta_cap is
- * read in TIDE_MODE_CAPPED only and must be >= 1. */
+ * read in TIDE_MODE_CAPPED (>= 1) and TIDE_MODE_BULK (>= 0, 0 = no cap). */
 TIDE_API tide_status_t tide_layout_set_mode(tide_layout_t layout, tide_mode_t mode, int32_t cta_cap);
 
 /* Grid and block size the next launch of `op` will use under the current

@@ -12,6 +12,8 @@
 // shards delivered straight into parameter storage; short-lived CTAs) and
 // §FSDP2通信开销的根源 (rank-major buffers, reduce-scatter semantics).
 #include <cuda_runtime.h>
+
+#include <algorithm>
 #include <stdint.h>
 
 #include "tide_internal.h"
@@ -327,6 +329,8 @@ __device__ __forceinline__ bool next_chunk(Cursor& c, const AgArgs& a, const voi
 
 }  // namespace bulk
 
+__device__ __forceinline__ uint64_t evict_first_policy_rs() { return bulk::evict_first_policy(); }
+
 template <bool TO_BUF>
 __global__ void __launch_bounds__(32) ag_bulk_kernel(AgArgs a) {
   constexpr int S = TIDE_BULK_STAGES;
@@ -387,6 +391,149 @@ __global__ void __launch_bounds__(32) ag_bulk_kernel(AgArgs a) {
     }
   }
   bulk::wait_all();
+}
+
+// ---------------------------------------------------------------- bulk-staged reduce-scatter
+// The reduce-scatter with its rank slices staged in shared memory by the TMA
+// engine.  Warp 0 is the producer: per chunk of E elements of a vector run it
+// issues N cp.async.bulk copies (one per rank, E*2 bytes each, spread over
+// its lanes) into one stage of a ring and one expect-tx on that stage's
+// "full" mbarrier.  Warps 1..8 consume: wait for "full", sum the N slices in
+// ascending rank order from shared memory (__fadd_rn, the same sequence as
+// the load/store kernel), write the fp32 results with streaming stores, and
+// release the stage on its "empty" mbarrier.  With ~192 KiB of slices in
+// flight per SM a CTA moves more bytes per SM than registers allow, which is
+// what a CTA-capped run is limited by.  Zero tiles, unaligned runs and the
+// < 8 element tails of vector runs are done by the consumers with plain
+// loads.  Every wait is bounded as in the bulk-copy placement.
+namespace bulk {
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(bar)) : "memory");
+}
+
+// Elements per rank slice for a stage of about `stage` bytes (a multiple of
+// 8, so every slice is a multiple of 16 bytes).
+__device__ __host__ __forceinline__ int rs_chunk_elems(int n, int stage) { return (stage / 2 / n) & ~7; }
+
+}  // namespace bulk
+
+constexpr int kRsBulkConsumerWarps = kRsBulkThreads / 32 - 1;
+constexpr int kRsBulkConsumers = kRsBulkConsumerWarps * 32;
+constexpr size_t kRsBulkRing = 196608;  // bytes of staged slices per CTA
+constexpr int kRsBulkMaxStages = 32;
+
+__device__ __forceinline__ void rs_scalar_run(const RsArgs& a, const Tile& tile, float* out, int e0,
+                                              int tid, int nthreads) {
+  const int N = a.num_ranks;
+  const uint16_t* const* g = a.gtab + (int64_t)tile.p * N;
+  for (int e = e0 + tid; e < tile.len; e += nthreads) {
+    float acc = 0.f;
+    for (int k = 0; k < N; ++k) acc = __fadd_rn(acc, bf16_f32(ld_stream_u16(g[k] + tile.src + e)));
+    out[e] = __fmul_rn(acc, a.scale);
+  }
+}
+
+__global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
+  extern __shared__ __align__(128) unsigned char rs_smem[];
+  const int N = a.num_ranks;
+  const int E = bulk::rs_chunk_elems(N, a.stage_bytes);
+  const uint32_t slice = (uint32_t)E * 2;          // bytes per rank per chunk
+  const uint32_t stage_bytes = slice * (uint32_t)N;
+  const int S = min(kRsBulkMaxStages, (int)(kRsBulkRing / stage_bytes));
+  uint64_t* full = (uint64_t*)(rs_smem + (size_t)S * stage_bytes);
+  uint64_t* empty = full + S;
+  const uint16_t** ptrs = (const uint16_t**)(empty + S);  // producer's current sources
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      bulk::mbar_init(&full[s], 1);
+      bulk::mbar_init(&empty[s], kRsBulkConsumerWarps);
+    }
+    bulk::fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (a.test_stall_ns) {  // wait on a phase nothing completes: must run out
+    if (threadIdx.x == 0 && !bulk::mbar_wait(&full[0], 0, a.test_stall_ns)) atomicExch(a.err, kDevErrTimeout);
+    return;
+  }
+
+  if (warp == 0) {  // ---------------- producer
+    const uint64_t pol = evict_first_policy_rs();
+    int64_t j = 0;
+    for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+      const Tile tile = a.tiles[t];
+      if ((tile.flags & kTileZero) || !(tile.flags & kTileVec)) continue;
+      const int vec = tile.len & ~7;
+      if (vec == 0) continue;
+      __syncwarp();
+      for (int k = lane; k < N; k += 32) ptrs[k] = a.gtab[(int64_t)tile.p * N + k] + tile.src;
+      __syncwarp();
+      for (int off = 0; off < vec; off += E, ++j) {
+        const int n = min(E, vec - off);
+        const int s = (int)(j % S);
+        if (j >= S) {  // the consumers released this stage's previous chunk
+          int ok = lane == 0 ? (int)bulk::mbar_wait(&empty[s], (uint32_t)(((j / S) + 1) & 1), a.timeout_ns) : 0;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            if (lane == 0) atomicExch(a.err, kDevErrTimeout);
+            // loads issued into the ring may still land: wait (bounded) for them
+            for (int64_t k = (j >= S ? j - S : 0); k < j; ++k)
+              if (lane == 0) bulk::mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), a.timeout_ns);
+            return;
+          }
+        }
+        if (lane == 0) bulk::mbar_expect_tx(&full[s], (uint32_t)N * (uint32_t)n * 2u);
+        __syncwarp();
+        unsigned char* st = rs_smem + (size_t)s * stage_bytes;
+        for (int k = lane; k < N; k += 32)
+          bulk::g2s(st + (size_t)k * slice, ptrs[k] + off, (uint32_t)n * 2u, &full[s], pol);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int cid = threadIdx.x - 32;
+  int64_t j = 0;
+  for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+    const Tile tile = a.tiles[t];
+    float* __restrict__ out = a.stab[(int64_t)tile.r * a.num_params + tile.p] + tile.dst;
+    if (tile.flags & kTileZero) {
+      for (int e = cid; e < tile.len; e += kRsBulkConsumers) out[e] = 0.f;
+      continue;
+    }
+    if (!(tile.flags & kTileVec)) {
+      rs_scalar_run(a, tile, out, 0, cid, kRsBulkConsumers);
+      continue;
+    }
+    const int vec = tile.len & ~7;
+    for (int off = 0; off < vec; off += E, ++j) {
+      const int n = min(E, vec - off);
+      const int s = (int)(j % S);
+      if (!bulk::mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.timeout_ns)) {
+        atomicExch(a.err, kDevErrTimeout);
+        return;
+      }
+      const unsigned char* st = rs_smem + (size_t)s * stage_bytes;
+      for (int v = cid; v < (n >> 3); v += kRsBulkConsumers) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int k = 0; k < N; ++k) add8(acc, *(const uint4*)(st + (size_t)k * slice + 16 * v));
+        float* o = out + off + 8 * v;
+        st_stream(o, __fmul_rn(acc[0], a.scale), __fmul_rn(acc[1], a.scale), __fmul_rn(acc[2], a.scale),
+                  __fmul_rn(acc[3], a.scale));
+        st_stream(o + 4, __fmul_rn(acc[4], a.scale), __fmul_rn(acc[5], a.scale), __fmul_rn(acc[6], a.scale),
+                  __fmul_rn(acc[7], a.scale));
+      }
+      __syncwarp();
+      if (lane == 0) bulk::mbar_arrive(&empty[s]);
+    }
+    rs_scalar_run(a, tile, out, vec, cid, kRsBulkConsumers);  // < 8 element tail
+  }
 }
 
 // ---------------------------------------------------------------- all-gather input pack
@@ -517,6 +664,20 @@ cudaError_t ag_bulk_occupancy(int* blocks_per_sm) {
                                        (int)kBulkSmem);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, ag_bulk_kernel<false>, 32, kBulkSmem);
+}
+
+cudaError_t launch_rs_bulk(const RsArgs& a, int grid, cudaStream_t stream) {
+  if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
+  const int N = a.num_ranks;
+  if (bulk::rs_chunk_elems(N, a.stage_bytes) < 8) return cudaErrorInvalidValue;
+  const size_t stage_bytes = (size_t)bulk::rs_chunk_elems(N, a.stage_bytes) * 2 * N;
+  if (kRsBulkRing / stage_bytes < 2) return cudaErrorInvalidValue;
+  const int S = (int)std::min<size_t>(kRsBulkMaxStages, kRsBulkRing / stage_bytes);
+  const size_t smem = (size_t)S * stage_bytes + 16 * (size_t)S + 8 * (size_t)N;
+  cudaError_t e = cudaFuncSetAttribute(rs_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  rs_bulk_kernel<<<grid, kRsBulkThreads, smem, stream>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t pk_occupancy(int* blocks_per_sm) {

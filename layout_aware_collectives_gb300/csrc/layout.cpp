@@ -261,9 +261,11 @@ tide_status_t tide_layout_set_mode(tide_layout_t l, tide_mode_t mode, int32_t ct
     return set_error(TIDE_ERR_INVALID_ARG, "unknown mode");
   if (mode == TIDE_MODE_CAPPED && cta_cap < 1)
     return set_error(TIDE_ERR_INVALID_ARG, "cta_cap must be >= 1 in TIDE_MODE_CAPPED");
+  if (mode == TIDE_MODE_BULK && cta_cap < 0)
+    return set_error(TIDE_ERR_INVALID_ARG, "cta_cap must be >= 0 in TIDE_MODE_BULK");
   std::lock_guard<std::mutex> g(l->mu);
   l->mode = mode;
-  l->cta_cap = mode == TIDE_MODE_CAPPED ? cta_cap : 0;
+  l->cta_cap = (mode == TIDE_MODE_CAPPED || mode == TIDE_MODE_BULK) ? cta_cap : 0;
   return TIDE_OK;
 }
 

@@ -39,8 +39,14 @@ tide_status_t query_device(const tide_layout_s* l, DeviceShape* d) {
 
 int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int occ) {
   if (tiles <= 0) return 0;
-  const int64_t g = mode == TIDE_MODE_CAPPED ? (int64_t)cap : (int64_t)sms * occ;
+  const bool capped = mode == TIDE_MODE_CAPPED || (mode == TIDE_MODE_BULK && cap > 0);
+  const int64_t g = capped ? (int64_t)cap : (int64_t)sms * occ;
   return (int)std::min<int64_t>(tiles, g);
+}
+
+bool rs_uses_bulk(const tide_layout_s* l) {
+  // slices of at least 8 elements within a 64 KiB stage
+  return l->mode == TIDE_MODE_BULK && l->num_ranks <= kRsBulkMaxRanks / 2;
 }
 
 // Bind the layout to the current device on first use: query the SM count
@@ -237,7 +243,14 @@ tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, std:
   a.num_ranks = l->num_ranks;
   a.num_params = l->num_params;
   a.scale = scale;
-  cudaError_t e = launch_rs(a, grid_of(l, t1 - t0, l->rs_occ), l->mode == TIDE_MODE_CAPPED, stream);
+  a.err = l->d_err;
+  a.timeout_ns = TIDE_BULK_TIMEOUT_NS;
+  a.test_stall_ns = (uint64_t)l->test_stall_ns;
+  // measured on GB300: 4 KiB rank slices over every SM, 8 KiB when capped
+  a.stage_bytes = l->cta_cap > 0 ? 65536 : 32768;
+  cudaError_t e = rs_uses_bulk(l) ? launch_rs_bulk(a, grid_of(l, t1 - t0, 1), stream)
+                                  : launch_rs(a, grid_of(l, t1 - t0, l->rs_occ), l->mode == TIDE_MODE_CAPPED,
+                                              stream);
   if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter kernel launch");
   return mark_used(l, slot, stream);
 }
@@ -325,9 +338,11 @@ tide_status_t tide_layout_launch_shape(tide_layout_t l, tide_op_t op, int32_t* g
                         : op == TIDE_OP_PACK      ? (int64_t)l->pk_tiles.size()
                                                   : (int64_t)l->ag_tiles.size();
   const bool bulk = l->mode == TIDE_MODE_BULK && (op == TIDE_OP_AG || op == TIDE_OP_STAGE);
-  const int occ = rs_like ? d.rs_occ : op == TIDE_OP_PACK ? d.pk_occ : bulk ? d.bulk_occ : d.ag_occ;
+  const bool rs_bulk = rs_like && rs_uses_bulk(l);
+  const int occ = rs_bulk ? 1 : rs_like ? d.rs_occ : op == TIDE_OP_PACK ? d.pk_occ : bulk ? d.bulk_occ : d.ag_occ;
   *grid = l->mode == TIDE_MODE_COPY_ENGINE ? 0 : grid_for(tiles, l->mode, l->cta_cap, d.sms, occ);
-  *block = rs_like ? rs_block(capped) : op == TIDE_OP_PACK ? pk_block(capped) : bulk ? 32 : ag_block(capped);
+  *block = rs_bulk ? kRsBulkThreads : rs_like ? rs_block(capped) : op == TIDE_OP_PACK ? pk_block(capped)
+                   : bulk ? 32 : ag_block(capped);
   return TIDE_OK;
 }
 

@@ -67,6 +67,12 @@ struct RsArgs {
   int32_t num_ranks;
   int32_t num_params;
   float scale;
+  // bulk-staged kernel only (see AgArgs); stage_bytes: target bytes of one
+  // ring stage (the N rank slices of a chunk)
+  int32_t stage_bytes = 0;
+  int* err = nullptr;
+  uint64_t timeout_ns = 0;
+  uint64_t test_stall_ns = 0;
 };
 
 // All-gather input pack: stab[r * P + p] is rank r's fp32 shard of p (only
@@ -116,6 +122,11 @@ cudaError_t launch_stage(const AgArgs& a, int grid, bool fat, cudaStream_t strea
 // shared-memory ring of TIDE_BULK_STAGES x TIDE_BULK_CHUNK bytes.
 cudaError_t launch_ag_bulk(const AgArgs& a, int grid, bool to_buf, cudaStream_t stream);
 cudaError_t ag_bulk_occupancy(int* blocks_per_sm);
+// Bulk-staged reduce-scatter (TMA engine): one CTA per SM, rank slices staged
+// in shared memory by a producer warp; N <= kRsBulkMaxRanks.
+constexpr int kRsBulkMaxRanks = 1024;  // bulk RS runs for N <= kRsBulkMaxRanks / 2
+constexpr int kRsBulkThreads = 288;
+cudaError_t launch_rs_bulk(const RsArgs& a, int grid, cudaStream_t stream);
 cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, cudaStream_t stream);
 int rs_block(bool fat);
 int ag_block(bool fat);

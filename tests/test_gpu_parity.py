@@ -23,7 +23,7 @@ import layout_aware_collectives_gb300 as tide  # noqa: E402
 
 MODES = [("uncapped", tide.TIDE_MODE_UNCAPPED, 0)] + [
     (f"capped{c}", tide.TIDE_MODE_CAPPED, c) for c in (1, 2, 7, 8, 32)] + [
-    ("bulk", tide.TIDE_MODE_BULK, 0)]
+    ("bulk_cap3", tide.TIDE_MODE_BULK, 3), ("bulk", tide.TIDE_MODE_BULK, 0)]
 
 
 def run(job, rs_mode=None, ag_mode=None, scale=None):
@@ -303,6 +303,16 @@ def test_full_size_sampled_parity(name):
         run(job)
         assert torch.equal(job.shards[0][0], ref[0]) and torch.equal(job.shards[-1][-1], ref[1])
         gpu_checks.torch_check_rs(job)
+        # TMA bulk-staged reduce-scatter, capped and over every SM
+        for cap in (16, 0):
+            lay.set_mode(tide.TIDE_MODE_BULK, cap)
+            for row in job.shards:
+                for s in row:
+                    s.fill_(float("nan"))
+            run(job)
+            lay.check_device()
+            gpu_checks.torch_check_rs(job)
+            gpu_checks.torch_check_ag(job)
         del job
         torch.cuda.empty_cache()
 
@@ -359,8 +369,15 @@ def test_bounded_wait_timeout_is_reported(tiny_job):
         lay.check_device()
     assert e.value.status == tide.TIDE_ERR_TIMEOUT
     lay.check_device()  # cleared
+    # the bulk-staged reduce-scatter's waits too
+    lay.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), job.wl.scale)
+    with pytest.raises(tide.TideError) as e:
+        lay.check_device()
+    assert e.value.status == tide.TIDE_ERR_TIMEOUT
     lay.set_test_stall(0)
     job.reset_outputs()
     lay.place(job.gathered, job.param_ptrs())
+    lay.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), job.wl.scale)
     lay.check_device()
     gpu_checks.full_check_ag(job)
+    gpu_checks.full_check_rs(job)

@@ -425,7 +425,12 @@ def run_tide(args):
     if not args.no_stock:
         out["stock_fsdp2"] = run_stock(job, wl, stream, rs_avg, ag_avg)
     if not args.no_e2e:
-        out["e2e"] = run_e2e(tide, layout, job, wl, stream, K, world)
+        try:
+            out["e2e"] = run_e2e(tide, layout, job, wl, stream, K, world)
+        except (RuntimeError, torch.OutOfMemoryError) as e:  # pinned host memory can run out
+            torch.cuda.synchronize()
+            out["e2e"] = {"value": None, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0, "unavailable": f"{type(e).__name__}: {e}"[:300]}
     if not args.no_interference:
         out["interference"] = run_interference(tide, layout, job, wl, props)
     layout.set_mode(tide.TIDE_MODE_UNCAPPED)

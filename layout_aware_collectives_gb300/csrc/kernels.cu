@@ -45,6 +45,14 @@ __device__ __forceinline__ void st_stream(float* p, float a, float b, float c, f
                : "memory");
 }
 
+// Plain 16-byte store / load (write-back, normal L2 priority).
+__device__ __forceinline__ void st_plain(void* p, uint4 v) { *(uint4*)p = v; }
+__device__ __forceinline__ uint4 ld_plain(const void* p) { return *(const uint4*)p; }
+
+#ifndef TIDE_AG_STREAMING  // 1: the placement copy uses streaming stores and no-allocate loads
+#define TIDE_AG_STREAMING 1
+#endif
+
 __device__ __forceinline__ void st_stream(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
@@ -195,10 +203,17 @@ __global__ void __launch_bounds__(THREADS) ag_kernel(AgArgs a) {
         uint4 d[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (v0 + u * THREADS < nvec) d[u] = ld_stream(src + 8 * (v0 + u * THREADS));
+          if (v0 + u * THREADS < nvec)
+            d[u] = TIDE_AG_STREAMING ? ld_stream(src + 8 * (v0 + u * THREADS))
+                                     : ld_plain(src + 8 * (v0 + u * THREADS));
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (v0 + u * THREADS < nvec) st_stream(dst + 8 * (v0 + u * THREADS), d[u]);
+          if (v0 + u * THREADS < nvec) {
+            if (TIDE_AG_STREAMING)
+              st_stream(dst + 8 * (v0 + u * THREADS), d[u]);
+            else
+              st_plain(dst + 8 * (v0 + u * THREADS), d[u]);
+          }
       }
       for (int e = 8 * nvec + threadIdx.x; e < tile.len; e += THREADS) dst[e] = ld_stream_u16(src + e);
     } else {

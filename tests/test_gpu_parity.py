@@ -381,3 +381,36 @@ def test_bounded_wait_timeout_is_reported(tiny_job):
     lay.check_device()
     gpu_checks.full_check_ag(job)
     gpu_checks.full_check_rs(job)
+
+
+def test_two_host_threads_share_a_layout(tiny_job):
+    """Calls from two host threads on two streams with their own outputs
+    (the layout serialises the host side; the streams run independently)."""
+    import threading
+
+    job = tiny_job
+    other = DeviceJob(job.wl, job.layout, fill=False)
+    other.grads, other.gathered = job.grads, job.gathered
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    errors = []
+
+    def work(j, s):
+        try:
+            for _ in range(20):
+                j.layout.reduce_scatter(j.grad_ptrs(), j.shard_ptrs(), j.wl.scale, stream=s)
+                j.layout.place(j.gathered, j.param_ptrs(), stream=s)
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    ts = [threading.Thread(target=work, args=(j, s)) for j, s in zip((job, other), streams)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for j in (job, other):
+        gpu_checks.full_check_rs(j)
+        gpu_checks.full_check_ag(j)

@@ -110,6 +110,11 @@ tide_status_t acquire_table(tide_layout_s* l, std::vector<uintptr_t>& key,
   if (hit) {
     if (hit->upload_stream != stream)
       TIDE_CUDA(cudaStreamWaitEvent(stream, hit->upload_ev, 0), "cudaStreamWaitEvent");
+    // One event tracks the slot's last reader, so a reader on another stream
+    // is ordered after the previous one: the event then covers both, and an
+    // eviction that waits on it cannot overwrite a table still being read.
+    if (hit->use_recorded && hit->use_stream != stream)
+      TIDE_CUDA(cudaStreamWaitEvent(stream, hit->use_ev, 0), "cudaStreamWaitEvent");
     *out = hit;
     return TIDE_OK;
   }
@@ -125,6 +130,8 @@ tide_status_t acquire_table(tide_layout_s* l, std::vector<uintptr_t>& key,
   // from the staging buffer, must be done before either is overwritten.
   if (s->used) TIDE_CUDA(cudaEventSynchronize(s->use_ev), "cudaEventSynchronize");
   s->used = false;
+  s->use_stream = nullptr;
+  s->use_recorded = false;
   const size_t n = std::max<size_t>(1, entries.size());
   if (s->capacity < n) {
     if (s->d_table) cudaFree(s->d_table);
@@ -154,6 +161,8 @@ tide_status_t acquire_table(tide_layout_s* l, std::vector<uintptr_t>& key,
 tide_status_t mark_used(tide_layout_s* l, PtrSlot* s, cudaStream_t stream) {
   s->last_use = ++l->use_counter;
   TIDE_CUDA(cudaEventRecord(s->use_ev, stream), "cudaEventRecord");
+  s->use_stream = stream;
+  s->use_recorded = true;
   return TIDE_OK;
 }
 

@@ -146,6 +146,8 @@ struct PtrSlot {
   cudaEvent_t upload_ev = nullptr;
   cudaEvent_t use_ev = nullptr;
   cudaStream_t upload_stream = nullptr;
+  cudaStream_t use_stream = nullptr;  // stream of the last kernel that read the table
+  bool use_recorded = false;          // use_ev / use_stream are set (stream 0 is a valid stream)
   bool used = false;
   uint64_t last_use = 0;
 };

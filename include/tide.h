@@ -56,7 +56,8 @@
  *    TIDE_ERR_UNSUPPORTED for a mode that an operation does not have,
  *    TIDE_ERR_CUDA when the CUDA runtime reports an error (the message is
  *    kept per host thread, see tide_last_error()).  On any error nothing is
- *    enqueued on the stream.
+ *    enqueued on the stream.  A bounded wait that runs out inside a
+ *    TIDE_MODE_BULK kernel is reported later, by tide_layout_check_device.
  */
 #ifndef TIDE_H
 #define TIDE_H
@@ -81,7 +82,7 @@ typedef enum {
   TIDE_ERR_MISALIGNED = 2,
   TIDE_ERR_UNSUPPORTED = 3,
   TIDE_ERR_CUDA = 4,
-  TIDE_ERR_TIMEOUT = 5, /* reserved for bounded device-side waits */
+  TIDE_ERR_TIMEOUT = 5, /* a bounded device wait ran out (tide_layout_check_device) */
   TIDE_ERR_OUT_OF_MEMORY = 6
 } tide_status_t;
 
@@ -90,11 +91,14 @@ typedef enum {
   TIDE_MODE_UNCAPPED = 0,
   /* Persistent kernels with at most `cta_cap` CTAs looping over the tile
    * list: the short-lived-CTA budget of "TIDE的设计思路", trading bandwidth
-   * for SM time left to concurrent compute. */
+   * for SM time left to concurrent compute.  Each CTA is 1024 threads wide
+   * (an SM hosting one is lost to full-SM compute kernels anyway, so it
+   * keeps a whole SM's loads in flight). */
   TIDE_MODE_CAPPED = 1,
-  /* Placement through the copy engines (cudaMemcpy2DAsync, no SM use), the
-   * copy-engine path of "TIDE的设计思路".  Reduce-scatter has no copy-engine
-   * form: it returns TIDE_ERR_UNSUPPORTED in this mode. */
+  /* Placement and Slot-Reuse staging through the copy engines
+   * (cudaMemcpy2DAsync, no SM use), the copy-engine path of "TIDE的设计思路".
+   * The reduce-scatter forms and the pack have no copy-engine form: they
+   * return TIDE_ERR_UNSUPPORTED in this mode. */
   TIDE_MODE_COPY_ENGINE = 2,
   /* The TMA bulk-copy engine (cp.async.bulk, mbarriers, every wait bounded;
    * see tide_layout_check_device).  Placement and staging: global -> shared

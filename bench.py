@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--mode", default="uncapped", choices=["uncapped", "capped", "bulk"],
                     help="kernel mode of the timed step")
     ap.add_argument("--cap", type=int, default=0, help="CTA cap for --mode capped / bulk")
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     return ap.parse_args()
 
 
@@ -310,8 +311,17 @@ def run_reference(args):
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(out))
+    emit(out, args)
     return 0
+
+
+def emit(out, args):
+    """The one JSON line on stdout, optionally appended to --out."""
+    line = json.dumps(out)
+    print(line)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(line + "\n")
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -437,7 +447,7 @@ def run_tide(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, 10.0)
     if rank == 0:
-        print(json.dumps(out))
+        emit(out, args)
     layout.close()
     if world > 1:
         import torch.distributed as dist

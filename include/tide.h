@@ -169,8 +169,16 @@ TIDE_API tide_status_t tide_layout_valid_rows(tide_layout_t layout, int32_t p, i
 TIDE_API tide_status_t tide_layout_chunk_rows(tide_layout_t layout, int32_t p, int64_t* rows);
 
 /* Select how the compute calls run (default TIDE_MODE_UNCAPPED).  cta_cap is
- * read in TIDE_MODE_CAPPED (>= 1) and TIDE_MODE_BULK (>= 0, 0 = no cap). */
+ * read in TIDE_MODE_CAPPED (>= 1) and TIDE_MODE_BULK (>= 0, 0 = no cap).
+ * A new layout starts in the mode named by the environment variable
+ * TIDE_MODE ("uncapped", "capped", "copy_engine" or "bulk", with the cap in
+ * TIDE_CTA_CAP) when it is set to a valid choice.  TIDE_TILE_BYTES (4096 ..
+ * 16777216) sets the bf16 bytes read per reduce-scatter tile (default 256
+ * KiB) of layouts created afterwards. */
 TIDE_API tide_status_t tide_layout_set_mode(tide_layout_t layout, tide_mode_t mode, int32_t cta_cap);
+
+/* Current mode and CTA cap (host-only). */
+TIDE_API tide_status_t tide_layout_get_mode(tide_layout_t layout, tide_mode_t* mode, int32_t* cta_cap);
 
 /* Grid and block size the next launch of `op` will use under the current
  * mode, for the device that is current (grid 0 means no kernel: an empty

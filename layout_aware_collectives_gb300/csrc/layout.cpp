@@ -8,6 +8,8 @@
 // "FSDP通信终局：TIDE零拷贝集合通信优化" §FSDP2通信开销的根源.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <algorithm>
 #include <new>
@@ -24,11 +26,22 @@ bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow
 
 int64_t roundup(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-// Elements per reduce-scatter tile: TIDE_RS_TILE_READ_BYTES (256 KiB) of
-// bf16 reads across the N ranks, at least one full CTA pass (8 elements per
-// thread).
+// bf16 bytes read per reduce-scatter tile: TIDE_RS_TILE_READ_BYTES, or the
+// TIDE_TILE_BYTES environment variable (4 KiB .. 16 MiB) when set.
+int64_t rs_tile_read_bytes() {
+  const char* e = getenv("TIDE_TILE_BYTES");
+  if (e && *e) {
+    char* end = nullptr;
+    const long long v = strtoll(e, &end, 10);
+    if (end && *end == '\0' && v >= 4096 && v <= (16ll << 20)) return (int64_t)v;
+  }
+  return TIDE_RS_TILE_READ_BYTES;
+}
+
+// Elements per reduce-scatter tile: rs_tile_read_bytes() of bf16 reads across
+// the N ranks, at least one full CTA pass (8 elements per thread).
 int64_t rs_tile_elems(int32_t n) {
-  int64_t t = (int64_t)TIDE_RS_TILE_READ_BYTES / 2 / n;
+  int64_t t = rs_tile_read_bytes() / 2 / n;
   t = std::max<int64_t>(8 * TIDE_RS_THREADS, std::min<int64_t>(65536, t));
   return t / 8 * 8;
 }
@@ -170,6 +183,23 @@ tide_status_t create(int32_t num_params, const int32_t* ndims, const int64_t* di
     delete l;
     return set_error(TIDE_ERR_OUT_OF_MEMORY, "host allocation of the tile lists failed");
   }
+  // initial mode from the environment (TIDE_MODE, TIDE_CTA_CAP); anything
+  // unrecognised leaves the default
+  if (const char* m = getenv("TIDE_MODE")) {
+    const char* c = getenv("TIDE_CTA_CAP");
+    const long cap = c ? strtol(c, nullptr, 10) : 0;
+    if (!strcmp(m, "uncapped")) {
+      l->mode = TIDE_MODE_UNCAPPED;
+    } else if (!strcmp(m, "capped") && cap >= 1 && cap <= (1l << 30)) {
+      l->mode = TIDE_MODE_CAPPED;
+      l->cta_cap = (int32_t)cap;
+    } else if (!strcmp(m, "copy_engine")) {
+      l->mode = TIDE_MODE_COPY_ENGINE;
+    } else if (!strcmp(m, "bulk") && cap >= 0 && cap <= (1l << 30)) {
+      l->mode = TIDE_MODE_BULK;
+      l->cta_cap = (int32_t)cap;
+    }
+  }
   *out = l;
   return TIDE_OK;
 }
@@ -266,6 +296,14 @@ tide_status_t tide_layout_set_mode(tide_layout_t l, tide_mode_t mode, int32_t ct
   std::lock_guard<std::mutex> g(l->mu);
   l->mode = mode;
   l->cta_cap = (mode == TIDE_MODE_CAPPED || mode == TIDE_MODE_BULK) ? cta_cap : 0;
+  return TIDE_OK;
+}
+
+tide_status_t tide_layout_get_mode(tide_layout_t l, tide_mode_t* mode, int32_t* cta_cap) {
+  if (!l || !mode || !cta_cap) return set_error(TIDE_ERR_INVALID_ARG, "NULL argument");
+  std::lock_guard<std::mutex> g(l->mu);
+  *mode = l->mode;
+  *cta_cap = l->cta_cap;
   return TIDE_OK;
 }
 

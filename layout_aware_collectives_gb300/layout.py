@@ -42,6 +42,9 @@ class Layout:
     def launch_shape(self, op: int):
         return _t.tide_layout_launch_shape(self.handle, op)
 
+    def get_mode(self):
+        return _t.tide_layout_get_mode(self.handle)
+
     def set_mode(self, mode: int, cta_cap: int = 0) -> None:
         _t.tide_layout_set_mode(self.handle, mode, cta_cap)
 

@@ -72,6 +72,7 @@ _sig("tide_layout_param_offset", _st, _vp, ctypes.c_int32, _i64p)
 _sig("tide_layout_valid_rows", _st, _vp, ctypes.c_int32, ctypes.c_int32, _i64p)
 _sig("tide_layout_chunk_rows", _st, _vp, ctypes.c_int32, _i64p)
 _sig("tide_layout_set_mode", _st, _vp, ctypes.c_int, ctypes.c_int32)
+_sig("tide_layout_get_mode", _st, _vp, _i32p, _i32p)
 _sig("tide_layout_launch_shape", _st, _vp, ctypes.c_int, _i32p, _i32p)
 _sig("tide_layout_tiles", _st, _vp, ctypes.c_int, _vp, ctypes.c_int64, _i64p)
 _sig("tide_rs_bf16_to_fp32", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
@@ -225,6 +226,13 @@ def tide_layout_chunk_rows(layout, p: int) -> int:
 
 def tide_layout_set_mode(layout, mode: int, cta_cap: int = 0) -> None:
     _check(_lib.tide_layout_set_mode(layout, mode, cta_cap), "tide_layout_set_mode")
+
+
+def tide_layout_get_mode(layout):
+    """(mode, cta_cap) of the layout."""
+    m, c = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(_lib.tide_layout_get_mode(layout, ctypes.byref(m), ctypes.byref(c)), "tide_layout_get_mode")
+    return m.value, c.value
 
 
 def tide_layout_launch_shape(layout, op: int):

@@ -276,3 +276,28 @@ def test_staged_tiles_read_slot_offsets(n, shapes, align):
     for p, r, src, dst, ln, flags in st:
         if not flags & 1:
             assert src == r * S + offs[p] + dst
+
+
+def test_environment_overrides(monkeypatch):
+    """TIDE_MODE / TIDE_CTA_CAP set a new layout's mode; TIDE_TILE_BYTES its
+    reduce-scatter tile size; invalid values leave the defaults."""
+    shapes = [(4096, 512)]
+    with tide.Layout(shapes, 8) as lay:
+        assert lay.get_mode() == (tide.TIDE_MODE_UNCAPPED, 0)
+        base = len(lay.tiles(tide.TIDE_OP_RS))
+    monkeypatch.setenv("TIDE_MODE", "capped")
+    monkeypatch.setenv("TIDE_CTA_CAP", "12")
+    monkeypatch.setenv("TIDE_TILE_BYTES", str(64 * 1024))
+    with tide.Layout(shapes, 8) as lay:
+        assert lay.get_mode() == (tide.TIDE_MODE_CAPPED, 12)
+        assert len(lay.tiles(tide.TIDE_OP_RS)) == 4 * base
+    monkeypatch.setenv("TIDE_MODE", "bulk")
+    monkeypatch.setenv("TIDE_CTA_CAP", "0")
+    with tide.Layout(shapes, 8) as lay:
+        assert lay.get_mode() == (tide.TIDE_MODE_BULK, 0)
+    monkeypatch.setenv("TIDE_MODE", "capped")
+    monkeypatch.setenv("TIDE_CTA_CAP", "0")  # invalid cap: default mode
+    monkeypatch.setenv("TIDE_TILE_BYTES", "12")  # out of range: default tiles
+    with tide.Layout(shapes, 8) as lay:
+        assert lay.get_mode() == (tide.TIDE_MODE_UNCAPPED, 0)
+        assert len(lay.tiles(tide.TIDE_OP_RS)) == base

@@ -45,8 +45,11 @@
  *    and keeps it alive until the work enqueued on `stream` completes.
  *  - Compute calls are asynchronous with respect to the host and never
  *    synchronise the device.  The first compute call of a layout uploads its
- *    tables to the device (allocating them); make one call before capturing
- *    a stream into a CUDA graph.
+ *    tables to the device (allocating them), and the first call with a new
+ *    set of pointers uploads that pointer table; after one such call on a
+ *    stream, the same calls with the same pointers can be captured from that
+ *    stream into a CUDA graph and replayed (tested for the reduce-scatter
+ *    and the placement).
  *  - A layout may be used from several host threads (calls are serialised
  *    internally).  Calls on different streams that write the same output
  *    buffers race, as any two kernels would.

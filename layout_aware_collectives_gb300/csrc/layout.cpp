@@ -47,6 +47,17 @@ int64_t rs_tile_elems(int32_t n) {
 }
 constexpr int64_t kAgTileElems = TIDE_AG_TILE_ELEMS;  // 64 KiB read + 64 KiB written
 constexpr int64_t kZeroTileElems = 65536;  // padding fill
+// Small layouts: shrink tiles until a list has about this many (8 per SM of
+// a 152-SM GPU), never below one CTA pass, so small jobs still spread over
+// the whole GPU.
+constexpr int64_t kMinTiles = 1216;
+constexpr int64_t kMinTileElems = 8 * 256;
+
+int64_t fit_tile(int64_t t, int64_t total_elems) {
+  const int64_t want = (total_elems + kMinTiles - 1) / kMinTiles;
+  if (want >= t) return t;
+  return std::max<int64_t>(kMinTileElems, (want + 7) / 8 * 8);
+}
 
 // Split [0, n) into near-equal runs of at most `t` elements, each run but
 // the last a multiple of 8 elements.
@@ -60,7 +71,10 @@ void split_runs(int64_t n, int64_t t, F&& emit) {
 
 void build_tiles(tide_layout_s* l) {
   const int32_t N = l->num_ranks;
-  const int64_t T = rs_tile_elems(N);
+  int64_t total = 0;  // elements of every rank's padded shards
+  for (int32_t p = 0; p < l->num_params; ++p) total += l->chunk[p] * l->inner[p] * N;
+  const int64_t T = fit_tile(rs_tile_elems(N), total);
+  const int64_t TA = fit_tile(kAgTileElems, total);
   l->rs_tiles.clear();
   l->ag_tiles.clear();
   l->pk_tiles.clear();
@@ -98,13 +112,13 @@ void build_tiles(tide_layout_s* l) {
         if (t.dst % 4 == 0) t.flags |= kTileVec;
         l->st_tiles.push_back(t);
       });
-      split_runs(seg, kAgTileElems, [&](int64_t s, int64_t n) {
+      split_runs(seg, TA, [&](int64_t s, int64_t n) {
         Tile t{ag_src + s, rs_src + s, (int32_t)n, p, r, 0u};
         if (t.src % 8 == 0 && t.dst % 8 == 0) t.flags |= kTileVec;
         l->ag_tiles.push_back(t);
       });
       // pack: the whole padded shard (padding rows are part of the AG input)
-      split_runs(c * inner, kAgTileElems, [&](int64_t s, int64_t n) {
+      split_runs(c * inner, TA, [&](int64_t s, int64_t n) {
         Tile t{s, ag_src + s, (int32_t)n, p, r, 0u};
         if (t.src % 4 == 0 && t.dst % 8 == 0) t.flags |= kTileVec;
         l->pk_tiles.push_back(t);

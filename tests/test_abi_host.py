@@ -281,7 +281,7 @@ def test_staged_tiles_read_slot_offsets(n, shapes, align):
 def test_environment_overrides(monkeypatch):
     """TIDE_MODE / TIDE_CTA_CAP set a new layout's mode; TIDE_TILE_BYTES its
     reduce-scatter tile size; invalid values leave the defaults."""
-    shapes = [(4096, 512)]
+    shapes = [(65536, 512)]  # large enough that small-layout tile shrinking stays out of it
     with tide.Layout(shapes, 8) as lay:
         assert lay.get_mode() == (tide.TIDE_MODE_UNCAPPED, 0)
         base = len(lay.tiles(tide.TIDE_OP_RS))
@@ -301,3 +301,16 @@ def test_environment_overrides(monkeypatch):
     with tide.Layout(shapes, 8) as lay:
         assert lay.get_mode() == (tide.TIDE_MODE_UNCAPPED, 0)
         assert len(lay.tiles(tide.TIDE_OP_RS)) == base
+
+
+def test_small_layouts_spread_over_the_gpu():
+    """A small layout gets tiles small enough to fill ~1216 CTA slots; a
+    large one keeps the full-size tiles."""
+    import synth
+
+    with tide.Layout(synth.tiny().shapes, 4) as lay:
+        for op in (tide.TIDE_OP_RS, tide.TIDE_OP_AG, tide.TIDE_OP_PACK):
+            assert len(lay.tiles(op)) >= 300
+    with tide.Layout([(8192, 8192)], 8) as lay:
+        t = lay.tiles(tide.TIDE_OP_RS)
+        assert t[:, 4].max() == 16384  # 256 KiB of bf16 reads over 8 ranks

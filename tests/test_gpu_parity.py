@@ -414,3 +414,31 @@ def test_two_host_threads_share_a_layout(tiny_job):
     for j in (job, other):
         gpu_checks.full_check_rs(j)
         gpu_checks.full_check_ag(j)
+
+
+def test_cuda_graph_capture_of_the_step(tiny_job):
+    """After a first call (which sets the layout up on the device), the
+    reduce-scatter and placement calls can be captured into a CUDA graph and
+    replayed; the replay gives the oracle's result."""
+    job = tiny_job
+    lay = job.layout
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g_ptrs, s_ptrs, p_ptrs = (tide.PointerTable(job.grad_ptrs()), tide.PointerTable(job.shard_ptrs()),
+                              tide.PointerTable(job.param_ptrs()))
+    lay.reduce_scatter(g_ptrs, s_ptrs, job.wl.scale, stream=s)
+    lay.place(job.gathered, p_ptrs, stream=s)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        lay.reduce_scatter(g_ptrs, s_ptrs, job.wl.scale, stream=s)
+        lay.place(job.gathered, p_ptrs, stream=s)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        job.reset_outputs()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        gpu_checks.full_check_rs(job)
+        gpu_checks.full_check_ag(job)
+        assert job.guards_intact()

@@ -48,8 +48,8 @@
  *    tables to the device (allocating them), and the first call with a new
  *    set of pointers uploads that pointer table; after one such call on a
  *    stream, the same calls with the same pointers can be captured from that
- *    stream into a CUDA graph and replayed (tested for the reduce-scatter
- *    and the placement).
+ *    stream into a CUDA graph and replayed (tested for tide_rs_bf16_to_fp32
+ *    and tide_ag_place).
  *  - A layout may be used from several host threads (calls are serialised
  *    internally).  Calls on different streams that write the same output
  *    buffers race, as any two kernels would.

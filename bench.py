@@ -404,9 +404,10 @@ def run_tide(args):
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": round(step_ms, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "num_ranks": wl.num_ranks, "num_params": wl.num_params,
                    "psi": wl.psi, "rs_bytes": rs_bytes, "ag_bytes": ag_bytes,
+                   "io": "bf16 gradients -> fp32 shards (fp32 sums); bf16 placement (bit copy)",
                    "l2": "flushed between steps" if small else
                    f"inputs larger than L2 ({(rs_bytes + ag_bytes) / 1e9:.1f} GB per step)",
                    "mode": args.mode + (f" cap {args.cap}" if args.cap else ""),

@@ -49,8 +49,29 @@ bool rs_uses_bulk(const tide_layout_s* l) {
   return l->mode == TIDE_MODE_BULK && l->num_ranks <= kRsBulkMaxRanks / 2;
 }
 
+void release_device(tide_layout_s* l) {
+  for (PtrSlot& s : l->slots) {
+    if (s.use_ev && s.used) cudaEventSynchronize(s.use_ev);
+    if (s.d_table) cudaFree(s.d_table);
+    if (s.h_staging) cudaFreeHost(s.h_staging);
+    if (s.upload_ev) cudaEventDestroy(s.upload_ev);
+    if (s.use_ev) cudaEventDestroy(s.use_ev);
+    s = PtrSlot();
+  }
+  Tile** lists[4] = {&l->d_rs_tiles, &l->d_ag_tiles, &l->d_pk_tiles, &l->d_st_tiles};
+  for (Tile** t : lists) {
+    if (*t) cudaFree(*t);
+    *t = nullptr;
+  }
+  if (l->d_err) cudaFree(l->d_err);
+  l->d_err = nullptr;
+}
+
+tide_status_t bind_device(tide_layout_s* l, int dev);
+
 // Bind the layout to the current device on first use: query the SM count
-// and occupancy, upload the tile lists.
+// and occupancy, upload the tile lists.  On failure everything allocated so
+// far is released and the layout stays unbound.
 tide_status_t ensure_device(tide_layout_s* l) {
   int dev = 0;
   TIDE_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
@@ -60,6 +81,12 @@ tide_status_t ensure_device(tide_layout_s* l) {
                                                  " but device " + std::to_string(dev) + " is current");
     return TIDE_OK;
   }
+  tide_status_t st = bind_device(l, dev);
+  if (st != TIDE_OK) release_device(l);
+  return st;
+}
+
+tide_status_t bind_device(tide_layout_s* l, int dev) {
   DeviceShape d;
   tide_status_t st = query_device(l, &d);
   if (st != TIDE_OK) return st;
@@ -316,18 +343,7 @@ void tide_layout_destroy(tide_layout_t l) {
     int cur = -1;
     cudaGetDevice(&cur);
     if (cur != l->device) cudaSetDevice(l->device);
-    for (PtrSlot& s : l->slots) {
-      if (s.use_ev && s.used) cudaEventSynchronize(s.use_ev);
-      if (s.d_table) cudaFree(s.d_table);
-      if (s.h_staging) cudaFreeHost(s.h_staging);
-      if (s.upload_ev) cudaEventDestroy(s.upload_ev);
-      if (s.use_ev) cudaEventDestroy(s.use_ev);
-    }
-    cudaFree(l->d_rs_tiles);
-    cudaFree(l->d_ag_tiles);
-    cudaFree(l->d_pk_tiles);
-    cudaFree(l->d_st_tiles);
-    cudaFree(l->d_err);
+    release_device(l);
     if (cur >= 0 && cur != l->device) cudaSetDevice(cur);
   }
   delete l;

@@ -49,7 +49,13 @@
  *    set of pointers uploads that pointer table; after one such call on a
  *    stream, the same calls with the same pointers can be captured from that
  *    stream into a CUDA graph and replayed (tested for tide_rs_bf16_to_fp32
- *    and tide_ag_place).
+ *    and tide_ag_place).  A pointer set used for the first time inside a
+ *    capture is refused (TIDE_ERR_UNSUPPORTED); the device table of a pointer
+ *    set used inside a capture is kept unchanged for the layout's lifetime
+ *    (at most 8 pointer sets per layout can be held that way), so destroy
+ *    the layout only once such graphs are no longer replayed.
+ *  - A failed CUDA call is reported through the status and cleared from the
+ *    runtime's per-thread last error.
  *  - A layout may be used from several host threads (calls are serialised
  *    internally).  Calls on different streams that write the same output
  *    buffers race, as any two kernels would.

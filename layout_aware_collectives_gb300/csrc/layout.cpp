@@ -226,6 +226,9 @@ tide_status_t set_error(tide_status_t st, const std::string& msg) {
 }
 
 tide_status_t cuda_fail(cudaError_t e, const char* what) {
+  // the error is reported through the status; clear the runtime's per-thread
+  // last error so it does not surface in the caller's next, unrelated check
+  cudaGetLastError();
   std::string m = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
   return set_error(e == cudaErrorMemoryAllocation ? TIDE_ERR_OUT_OF_MEMORY : TIDE_ERR_CUDA, m);
 }

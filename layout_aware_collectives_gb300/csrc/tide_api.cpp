@@ -49,9 +49,19 @@ bool rs_uses_bulk(const tide_layout_s* l) {
   return l->mode == TIDE_MODE_BULK && l->num_ranks <= kRsBulkMaxRanks / 2;
 }
 
+// True while `stream` is being captured into a CUDA graph.
+bool capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &st) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return st == cudaStreamCaptureStatusActive;
+}
+
 void release_device(tide_layout_s* l) {
   for (PtrSlot& s : l->slots) {
-    if (s.use_ev && s.used) cudaEventSynchronize(s.use_ev);
+    if (s.use_ev && s.use_recorded) cudaEventSynchronize(s.use_ev);
     if (s.d_table) cudaFree(s.d_table);
     if (s.h_staging) cudaFreeHost(s.h_staging);
     if (s.upload_ev) cudaEventDestroy(s.upload_ev);
@@ -65,6 +75,7 @@ void release_device(tide_layout_s* l) {
   }
   if (l->d_err) cudaFree(l->d_err);
   l->d_err = nullptr;
+  cudaGetLastError();  // leave no error of the clean-up behind
 }
 
 tide_status_t bind_device(tide_layout_s* l, int dev);
@@ -134,28 +145,40 @@ tide_status_t acquire_table(tide_layout_s* l, std::vector<uintptr_t>& key,
       hit = &s;
       break;
     }
+  const bool cap = capturing(stream);
   if (hit) {
-    if (hit->upload_stream != stream)
+    // Inside a capture the table was uploaded by an earlier call on this
+    // stream (required), and no host-side event is recorded or waited on.
+    if (!cap && hit->upload_stream != stream)
       TIDE_CUDA(cudaStreamWaitEvent(stream, hit->upload_ev, 0), "cudaStreamWaitEvent");
     // One event tracks the slot's last reader, so a reader on another stream
     // is ordered after the previous one: the event then covers both, and an
     // eviction that waits on it cannot overwrite a table still being read.
-    if (hit->use_recorded && hit->use_stream != stream)
+    if (!cap && hit->use_recorded && hit->use_stream != stream)
       TIDE_CUDA(cudaStreamWaitEvent(stream, hit->use_ev, 0), "cudaStreamWaitEvent");
     *out = hit;
     return TIDE_OK;
   }
-  PtrSlot* s = &l->slots[0];
+  if (cap)
+    return set_error(TIDE_ERR_UNSUPPORTED,
+                     "pointer set used for the first time inside a stream capture; make one call "
+                     "with these pointers on this stream before capturing");
+  PtrSlot* s = nullptr;  // a free slot, else the least recently used one no graph reads
   for (PtrSlot& c : l->slots) {
+    if (c.graph_pinned) continue;
     if (!c.used) {
       s = &c;
       break;
     }
-    if (c.last_use < s->last_use) s = &c;
+    if (!s || c.last_use < s->last_use) s = &c;
   }
+  if (!s)
+    return set_error(TIDE_ERR_UNSUPPORTED,
+                     "every pointer-table slot of this layout is read by a captured CUDA graph");
   // Kernels that read this slot's previous table, and its previous upload
   // from the staging buffer, must be done before either is overwritten.
-  if (s->used) TIDE_CUDA(cudaEventSynchronize(s->use_ev), "cudaEventSynchronize");
+  if (s->used && s->use_recorded) TIDE_CUDA(cudaEventSynchronize(s->use_ev), "cudaEventSynchronize");
+  if (s->used && !s->use_recorded) TIDE_CUDA(cudaEventSynchronize(s->upload_ev), "cudaEventSynchronize");
   s->used = false;
   s->use_stream = nullptr;
   s->use_recorded = false;
@@ -187,6 +210,10 @@ tide_status_t acquire_table(tide_layout_s* l, std::vector<uintptr_t>& key,
 
 tide_status_t mark_used(tide_layout_s* l, PtrSlot* s, cudaStream_t stream) {
   s->last_use = ++l->use_counter;
+  if (capturing(stream)) {  // a graph may replay this launch at any time from now on
+    s->graph_pinned = true;
+    return TIDE_OK;
+  }
   TIDE_CUDA(cudaEventRecord(s->use_ev, stream), "cudaEventRecord");
   s->use_stream = stream;
   s->use_recorded = true;

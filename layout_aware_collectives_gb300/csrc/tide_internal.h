@@ -148,6 +148,7 @@ struct PtrSlot {
   cudaStream_t upload_stream = nullptr;
   cudaStream_t use_stream = nullptr;  // stream of the last kernel that read the table
   bool use_recorded = false;          // use_ev / use_stream are set (stream 0 is a valid stream)
+  bool graph_pinned = false;          // read by a captured CUDA graph: never rewritten
   bool used = false;
   uint64_t last_use = 0;
 };

@@ -134,14 +134,51 @@ tide_status_t bind_device(tide_layout_s* l, int dev) {
   return TIDE_OK;
 }
 
+// Identity of a pointer-table request: the caller's raw pointer arrays (one
+// or two), with the operation tag and rank.  The hash is FNV-1a over the
+// pointer values; a hit is confirmed by comparing the arrays themselves.
+struct TableKey {
+  uintptr_t tag;
+  intptr_t rank;
+  const void* const* a;
+  size_t na;
+  const void* const* b;
+  size_t nb;
+  uint64_t hash;
+};
+
+TableKey make_key(uintptr_t tag, intptr_t rank, const void* const* a, size_t na, const void* const* b,
+                  size_t nb) {
+  uint64_t h = 1469598103934665603ull ^ (tag * 0x9E3779B97F4A7C15ull) ^ (uint64_t)rank;
+  for (size_t i = 0; i < na; ++i) h = (h ^ (uint64_t)(uintptr_t)a[i]) * 1099511628211ull;
+  for (size_t i = 0; i < nb; ++i) h = (h ^ (uint64_t)(uintptr_t)b[i]) * 1099511628211ull;
+  return TableKey{tag, rank, a, na, b, nb, h};
+}
+
+bool same_key(const PtrSlot& s, const TableKey& k) {
+  return s.used && s.hash == k.hash && s.tag == k.tag && s.rank == k.rank && s.na == k.na &&
+         s.nb == k.nb && (k.na == 0 || !std::memcmp(s.key.data(), k.a, k.na * sizeof(void*))) &&
+         (k.nb == 0 || !std::memcmp(s.key.data() + k.na, k.b, k.nb * sizeof(void*)));
+}
+
+// True when a slot already holds this exact pointer set: the pointers were
+// validated when the slot was filled, so a hit skips validation.
+bool cached(const tide_layout_s* l, const TableKey& key) {
+  for (const PtrSlot& s : l->slots)
+    if (same_key(s, key)) return true;
+  return false;
+}
+
 // Device copy of a pointer table, cached by content: steady-state training
-// passes the same buffers every step, so a hit costs a key comparison and a
-// stream-ordering wait.  `entries` is the table in device order.
-tide_status_t acquire_table(tide_layout_s* l, std::vector<uintptr_t>& key,
-                            const std::vector<void*>& entries, cudaStream_t stream, PtrSlot** out) {
+// passes the same buffers every step, so a hit costs a hash and array
+// comparison and, when the stream changed, a stream-ordering wait.  On a miss
+// `build(dst)` writes the n_entries table entries in device order.
+template <typename Build>
+tide_status_t acquire_table(tide_layout_s* l, const TableKey& key, size_t n_entries, Build&& build,
+                            cudaStream_t stream, PtrSlot** out) {
   PtrSlot* hit = nullptr;
   for (PtrSlot& s : l->slots)
-    if (s.used && s.key == key) {
+    if (same_key(s, key)) {
       hit = &s;
       break;
     }
@@ -182,7 +219,7 @@ tide_status_t acquire_table(tide_layout_s* l, std::vector<uintptr_t>& key,
   s->used = false;
   s->use_stream = nullptr;
   s->use_recorded = false;
-  const size_t n = std::max<size_t>(1, entries.size());
+  const size_t n = std::max<size_t>(1, n_entries);
   if (s->capacity < n) {
     if (s->d_table) cudaFree(s->d_table);
     if (s->h_staging) cudaFreeHost(s->h_staging);
@@ -194,15 +231,22 @@ tide_status_t acquire_table(tide_layout_s* l, std::vector<uintptr_t>& key,
               "cudaMallocHost(pointer table staging)");
     s->capacity = n;
   }
-  if (!entries.empty()) {
-    std::memcpy(s->h_staging, entries.data(), entries.size() * sizeof(void*));
-    TIDE_CUDA(cudaMemcpyAsync(s->d_table, s->h_staging, entries.size() * sizeof(void*),
-                              cudaMemcpyHostToDevice, stream),
+  if (n_entries) {
+    build(s->h_staging);
+    TIDE_CUDA(cudaMemcpyAsync(s->d_table, s->h_staging, n_entries * sizeof(void*), cudaMemcpyHostToDevice,
+                              stream),
               "upload of the pointer table");
   }
   TIDE_CUDA(cudaEventRecord(s->upload_ev, stream), "cudaEventRecord");
   s->upload_stream = stream;
-  s->key.swap(key);
+  s->tag = key.tag;
+  s->rank = key.rank;
+  s->hash = key.hash;
+  s->na = key.na;
+  s->nb = key.nb;
+  s->key.resize(key.na + key.nb);
+  if (key.na) std::memcpy(s->key.data(), key.a, key.na * sizeof(void*));
+  if (key.nb) std::memcpy(s->key.data() + key.na, key.b, key.nb * sizeof(void*));
   s->used = true;
   *out = s;
   return TIDE_OK;
@@ -287,17 +331,20 @@ using namespace tide;
 namespace tide {
 namespace {
 
-// Shared steps of the kernel entry points once arguments are validated: bind
-// the device, fetch the cached device pointer table, launch.
-tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, std::vector<uintptr_t>& key,
-                     const std::vector<void*>& entries, float scale, cudaStream_t stream) {
+// Shared steps of the reduce-scatter entry points once arguments are
+// validated: bind the device, fetch the cached device pointer table (built
+// by `build` on a miss: N*P source pointers param-major, then N*P shard
+// pointers rank-major), launch.
+template <typename Build>
+tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, const TableKey& key, Build&& build,
+                     float scale, cudaStream_t stream) {
   if (t1 <= t0) return TIDE_OK;
   tide_status_t st = ensure_device(l);
   if (st != TIDE_OK) return st;
-  PtrSlot* slot = nullptr;
-  st = acquire_table(l, key, entries, stream, &slot);
-  if (st != TIDE_OK) return st;
   const int64_t NP = (int64_t)l->num_ranks * l->num_params;
+  PtrSlot* slot = nullptr;
+  st = acquire_table(l, key, (size_t)(2 * NP), build, stream, &slot);
+  if (st != TIDE_OK) return st;
   RsArgs a;
   a.tiles = (staged ? l->d_st_tiles : l->d_rs_tiles) + t0;
   a.num_tiles = t1 - t0;
@@ -318,32 +365,38 @@ tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, std:
   return mark_used(l, slot, stream);
 }
 
-// Gradient table (param-major) + shard table (rank-major) for the RS kernel;
-// shard entries of ranks not written stay null and are never read.
-tide_status_t rs_tables(tide_layout_s* l, int32_t rank, const uint16_t* const* grads,
-                        float* const* shards, std::vector<uintptr_t>* key,
-                        std::vector<void*>* entries) {
+// Validation of N*P gradient pointers (rank-major) and of `nout` shard
+// pointers (all ranks, or one rank's P).
+tide_status_t check_rs_ptrs(const tide_layout_s* l, const uint16_t* const* grads, float* const* shards,
+                            int64_t nout) {
   const int32_t N = l->num_ranks, P = l->num_params;
-  for (int64_t i = 0; i < (int64_t)N * P; ++i) {
-    tide_status_t st = check_ptr(grads[i], l->d0[i % P] * l->inner[i % P], "grads", i);
+  for (int32_t k = 0; k < N; ++k)
+    for (int32_t p = 0; p < P; ++p) {
+      const int64_t i = (int64_t)k * P + p;
+      tide_status_t st = check_ptr(grads[i], l->d0[p] * l->inner[p], "grads", i);
+      if (st != TIDE_OK) return st;
+    }
+  for (int64_t i = 0, p = 0; i < nout; ++i, p = (p + 1 == P ? 0 : p + 1)) {
+    tide_status_t st = check_ptr(shards[i], l->shard_numel[p], "shards", i);
     if (st != TIDE_OK) return st;
   }
-  const int64_t nout = rank < 0 ? (int64_t)N * P : P;
-  for (int64_t i = 0; i < nout; ++i) {
-    tide_status_t st = check_ptr(shards[i], l->shard_numel[i % P], "shards", i);
-    if (st != TIDE_OK) return st;
-  }
-  entries->assign((size_t)2 * N * P, nullptr);
-  for (int32_t p = 0; p < P; ++p)
-    for (int32_t k = 0; k < N; ++k) (*entries)[(size_t)p * N + k] = (void*)grads[(size_t)k * P + p];
-  for (int64_t i = 0; i < nout; ++i)
-    (*entries)[(size_t)N * P + (rank < 0 ? i : (int64_t)rank * P + i)] = (void*)shards[i];
-  key->clear();
-  key->reserve(2 + entries->size());
-  key->push_back((uintptr_t)TIDE_OP_RS);
-  key->push_back((uintptr_t)(intptr_t)rank);
-  for (void* e : *entries) key->push_back((uintptr_t)e);
   return TIDE_OK;
+}
+
+// Device table of a reduce-scatter: gradients param-major, then the shard
+// table rank-major with the entries of ranks not written left null.
+void build_rs_table(const tide_layout_s* l, int32_t rank, const uint16_t* const* grads, float* const* shards,
+                    void** dst) {
+  const int32_t N = l->num_ranks, P = l->num_params;
+  const size_t NP = (size_t)N * P;
+  for (int32_t p = 0; p < P; ++p)
+    for (int32_t k = 0; k < N; ++k) dst[(size_t)p * N + k] = (void*)grads[(size_t)k * P + p];
+  if (rank < 0) {
+    std::memcpy(dst + NP, shards, NP * sizeof(void*));
+  } else {
+    std::memset(dst + NP, 0, NP * sizeof(void*));
+    std::memcpy(dst + NP + (size_t)rank * P, shards, (size_t)P * sizeof(void*));
+  }
 }
 
 // Placement (to_buf = false) or staging (to_buf = true) over the AG tile
@@ -406,11 +459,15 @@ tide_status_t tide_rs_bf16_to_fp32(tide_layout_t l, const uint16_t* const* grads
   std::lock_guard<std::mutex> g(l->mu);
   if (l->mode == TIDE_MODE_COPY_ENGINE)
     return set_error(TIDE_ERR_UNSUPPORTED, "reduce-scatter has no copy-engine mode");
-  std::vector<uintptr_t> key;
-  std::vector<void*> entries;
-  tide_status_t st = rs_tables(l, -1, grads, shards, &key, &entries);
-  if (st != TIDE_OK) return st;
-  return run_rs(l, false, 0, (int64_t)l->rs_tiles.size(), key, entries, scale, stream);
+  const int64_t NP = (int64_t)l->num_ranks * l->num_params;
+  const TableKey key = make_key(TIDE_OP_RS, -1, (const void* const*)grads, (size_t)NP,
+                                (const void* const*)shards, (size_t)NP);
+  if (!cached(l, key)) {
+    tide_status_t st = check_rs_ptrs(l, grads, shards, NP);
+    if (st != TIDE_OK) return st;
+  }
+  return run_rs(l, false, 0, (int64_t)l->rs_tiles.size(), key,
+                [&](void** dst) { build_rs_table(l, -1, grads, shards, dst); }, scale, stream);
 }
 
 tide_status_t tide_rs_bf16_to_fp32_rank(tide_layout_t l, int32_t rank, const uint16_t* const* grads,
@@ -422,11 +479,15 @@ tide_status_t tide_rs_bf16_to_fp32_rank(tide_layout_t l, int32_t rank, const uin
   std::lock_guard<std::mutex> g(l->mu);
   if (l->mode == TIDE_MODE_COPY_ENGINE)
     return set_error(TIDE_ERR_UNSUPPORTED, "reduce-scatter has no copy-engine mode");
-  std::vector<uintptr_t> key;
-  std::vector<void*> entries;
-  tide_status_t st = rs_tables(l, rank, grads, shards, &key, &entries);
-  if (st != TIDE_OK) return st;
-  return run_rs(l, false, l->rs_rank_begin[rank], l->rs_rank_begin[rank + 1], key, entries, scale, stream);
+  const int64_t NP = (int64_t)l->num_ranks * l->num_params;
+  const TableKey key = make_key(TIDE_OP_RS, rank, (const void* const*)grads, (size_t)NP,
+                                (const void* const*)shards, (size_t)l->num_params);
+  if (!cached(l, key)) {
+    tide_status_t st = check_rs_ptrs(l, grads, shards, l->num_params);
+    if (st != TIDE_OK) return st;
+  }
+  return run_rs(l, false, l->rs_rank_begin[rank], l->rs_rank_begin[rank + 1], key,
+                [&](void** dst) { build_rs_table(l, rank, grads, shards, dst); }, scale, stream);
 }
 
 tide_status_t tide_ag_place(tide_layout_t l, const uint16_t* gathered, uint16_t* const* params,
@@ -447,16 +508,11 @@ tide_status_t tide_ag_place(tide_layout_t l, const uint16_t* gathered, uint16_t*
   if (l->mode == TIDE_MODE_COPY_ENGINE)
     return copy_engine(l, const_cast<uint16_t*>(gathered), params, false, stream);
 
-  std::vector<uintptr_t> key;
-  key.reserve(1 + (size_t)P);
-  key.push_back((uintptr_t)TIDE_OP_AG);
-  std::vector<void*> entries((size_t)P);
-  for (int32_t p = 0; p < P; ++p) {
-    entries[p] = (void*)params[p];
-    key.push_back((uintptr_t)params[p]);
-  }
+  const TableKey key = make_key(TIDE_OP_AG, 0, (const void* const*)params, (size_t)P, nullptr, 0);
   PtrSlot* slot = nullptr;
-  st = acquire_table(l, key, entries, stream, &slot);
+  st = acquire_table(
+      l, key, (size_t)P, [&](void** dst) { std::memcpy(dst, params, (size_t)P * sizeof(void*)); }, stream,
+      &slot);
   if (st != TIDE_OK) return st;
 
   AgArgs a;
@@ -491,15 +547,19 @@ tide_status_t tide_ag_pack_bf16(tide_layout_t l, int32_t rank, const float* cons
   st = ensure_device(l);
   if (st != TIDE_OK) return st;
 
-  std::vector<void*> entries((size_t)N * P, nullptr);
-  for (int64_t i = 0; i < nin; ++i) entries[(size_t)(rank < 0 ? i : (int64_t)rank * P + i)] = (void*)shards[i];
-  std::vector<uintptr_t> key;
-  key.reserve(2 + entries.size());
-  key.push_back((uintptr_t)TIDE_OP_PACK);
-  key.push_back((uintptr_t)(intptr_t)rank);
-  for (void* e : entries) key.push_back((uintptr_t)e);
+  const TableKey key = make_key(TIDE_OP_PACK, rank, (const void* const*)shards, (size_t)nin, nullptr, 0);
   PtrSlot* slot = nullptr;
-  st = acquire_table(l, key, entries, stream, &slot);
+  st = acquire_table(
+      l, key, (size_t)N * P,
+      [&](void** dst) {  // rank-major; the entries of ranks not packed stay null
+        if (rank < 0) {
+          std::memcpy(dst, shards, (size_t)N * P * sizeof(void*));
+        } else {
+          std::memset(dst, 0, (size_t)N * P * sizeof(void*));
+          std::memcpy(dst + (size_t)rank * P, shards, (size_t)P * sizeof(void*));
+        }
+      },
+      stream, &slot);
   if (st != TIDE_OK) return st;
 
   PackArgs a;
@@ -531,16 +591,11 @@ tide_status_t tide_rs_stage_bf16(tide_layout_t l, const uint16_t* const* grads, 
   if (l->mode == TIDE_MODE_COPY_ENGINE)
     return copy_engine(l, slot, const_cast<uint16_t* const*>(grads), true, stream);
 
-  std::vector<uintptr_t> key;
-  key.reserve(1 + (size_t)P);
-  key.push_back((uintptr_t)TIDE_OP_STAGE);
-  std::vector<void*> entries((size_t)P);
-  for (int32_t p = 0; p < P; ++p) {
-    entries[p] = (void*)grads[p];
-    key.push_back((uintptr_t)grads[p]);
-  }
+  const TableKey key = make_key(TIDE_OP_STAGE, 0, (const void* const*)grads, (size_t)P, nullptr, 0);
   PtrSlot* ps = nullptr;
-  st = acquire_table(l, key, entries, stream, &ps);
+  st = acquire_table(
+      l, key, (size_t)P, [&](void** dst) { std::memcpy(dst, grads, (size_t)P * sizeof(void*)); }, stream,
+      &ps);
   if (st != TIDE_OK) return st;
   AgArgs a;
   a.tiles = l->d_ag_tiles;
@@ -565,22 +620,22 @@ tide_status_t tide_rs_staged_bf16_to_fp32(tide_layout_t l, const uint16_t* const
     tide_status_t st = check_ptr(slots[k], l->block_numel * N, "slots", k);
     if (st != TIDE_OK) return st;
   }
-  for (int64_t i = 0; i < (int64_t)N * P; ++i) {
-    tide_status_t st = check_ptr(shards[i], l->shard_numel[i % P], "shards", i);
+  for (int64_t i = 0, p = 0; i < (int64_t)N * P; ++i, p = (p + 1 == P ? 0 : p + 1)) {
+    tide_status_t st = check_ptr(shards[i], l->shard_numel[p], "shards", i);
     if (st != TIDE_OK) return st;
   }
   // the kernel's per-parameter source table points every parameter at the
   // slot bases; the staged tiles carry slot offsets r*S + o_p + s
-  std::vector<void*> entries((size_t)2 * N * P);
-  for (int32_t p = 0; p < P; ++p)
-    for (int32_t k = 0; k < N; ++k) entries[(size_t)p * N + k] = (void*)slots[k];
-  for (int64_t i = 0; i < (int64_t)N * P; ++i) entries[(size_t)N * P + i] = (void*)shards[i];
-  std::vector<uintptr_t> key;
-  key.reserve(2 + entries.size());
-  key.push_back((uintptr_t)TIDE_OP_STAGED_RS);
-  key.push_back(0);
-  for (void* e : entries) key.push_back((uintptr_t)e);
-  return run_rs(l, true, 0, (int64_t)l->st_tiles.size(), key, entries, scale, stream);
+  const TableKey key = make_key(TIDE_OP_STAGED_RS, 0, (const void* const*)slots, (size_t)N,
+                                (const void* const*)shards, (size_t)N * P);
+  return run_rs(
+      l, true, 0, (int64_t)l->st_tiles.size(), key,
+      [&](void** dst) {
+        for (int32_t p = 0; p < P; ++p)
+          for (int32_t k = 0; k < N; ++k) dst[(size_t)p * N + k] = (void*)slots[k];
+        std::memcpy(dst + (size_t)N * P, shards, (size_t)N * P * sizeof(void*));
+      },
+      scale, stream);
 }
 
 tide_status_t tide_layout_check_device(tide_layout_t l) {

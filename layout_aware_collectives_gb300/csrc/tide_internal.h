@@ -139,7 +139,13 @@ size_t rs_smem_bytes(int32_t num_ranks);
 
 // Device-side pointer table, cached by content.
 struct PtrSlot {
-  std::vector<uintptr_t> key;   // op tag followed by the host pointer table(s)
+  // identity of the cached table: tag (operation), rank, hash and the
+  // caller's raw pointer arrays back to back
+  uintptr_t tag = 0;
+  intptr_t rank = 0;
+  uint64_t hash = 0;
+  size_t na = 0, nb = 0;
+  std::vector<uintptr_t> key;
   void** d_table = nullptr;     // device copy
   void** h_staging = nullptr;   // pinned staging for the upload
   size_t capacity = 0;          // entries

@@ -105,8 +105,8 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
-        self.dev = device_index
+    def __init__(self, device: str):
+        self.dev = device
         self.lines = []
         self.proc = None
 
@@ -366,8 +366,9 @@ def run_tide(args):
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    clocks = ClockSampler(dev if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    # nvidia-smi -i takes an index, a UUID or a PCI id: pass the visible entry as is
+    visible = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    clocks = ClockSampler(visible[dev] if dev < len(visible) else str(dev))
     clocks.start()
     time.sleep(0.3)
     barrier(world)

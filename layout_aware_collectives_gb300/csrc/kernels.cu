@@ -184,9 +184,16 @@ __global__ void __launch_bounds__(THREADS, TIDE_RS_MIN_BLOCKS) rs_kernel(RsArgs 
 // gathered[r*S + o_p + ...] to params[p][r*c_p*inner_p + ...].  U 16-byte
 // vectors per thread are loaded before any is stored.  TO_BUF runs the same
 // copy backwards (Slot-Reuse staging of a gradient into the rank-major slot).
-template <int THREADS, int U, bool TO_BUF>
+// A CTA is WORKERS independent groups of THREADS / WORKERS threads, each
+// walking its own tiles (a capped-mode CTA is two tile-sized groups, so one
+// pass of each group covers a whole tile).
+template <int THREADS, int WORKERS, int U, bool TO_BUF>
 __global__ void __launch_bounds__(THREADS) ag_kernel(AgArgs a) {
-  for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+  constexpr int WT = THREADS / WORKERS;
+  static_assert(THREADS % WORKERS == 0 && WT % 32 == 0, "workers are whole warps");
+  const int lane = (int)threadIdx.x % WT;
+  for (int64_t t = (int64_t)blockIdx.x * WORKERS + (int)threadIdx.x / WT; t < a.num_tiles;
+       t += (int64_t)gridDim.x * WORKERS) {
     const Tile tile = a.tiles[t];
     const uint16_t* __restrict__ src;
     uint16_t* __restrict__ dst;
@@ -199,25 +206,25 @@ __global__ void __launch_bounds__(THREADS) ag_kernel(AgArgs a) {
     }
     if (tile.flags & kTileVec) {
       const int nvec = tile.len >> 3;
-      for (int v0 = threadIdx.x; v0 < nvec; v0 += U * THREADS) {
+      for (int v0 = lane; v0 < nvec; v0 += U * WT) {
         uint4 d[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (v0 + u * THREADS < nvec)
-            d[u] = TIDE_AG_STREAMING ? ld_stream(src + 8 * (v0 + u * THREADS))
-                                     : ld_plain(src + 8 * (v0 + u * THREADS));
+          if (v0 + u * WT < nvec)
+            d[u] = TIDE_AG_STREAMING ? ld_stream(src + 8 * (v0 + u * WT))
+                                     : ld_plain(src + 8 * (v0 + u * WT));
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (v0 + u * THREADS < nvec) {
+          if (v0 + u * WT < nvec) {
             if (TIDE_AG_STREAMING)
-              st_stream(dst + 8 * (v0 + u * THREADS), d[u]);
+              st_stream(dst + 8 * (v0 + u * WT), d[u]);
             else
-              st_plain(dst + 8 * (v0 + u * THREADS), d[u]);
+              st_plain(dst + 8 * (v0 + u * WT), d[u]);
           }
       }
-      for (int e = 8 * nvec + threadIdx.x; e < tile.len; e += THREADS) dst[e] = ld_stream_u16(src + e);
+      for (int e = 8 * nvec + lane; e < tile.len; e += WT) dst[e] = ld_stream_u16(src + e);
     } else {
-      for (int e = threadIdx.x; e < tile.len; e += THREADS) dst[e] = ld_stream_u16(src + e);
+      for (int e = lane; e < tile.len; e += WT) dst[e] = ld_stream_u16(src + e);
     }
   }
 }
@@ -568,17 +575,21 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // One tile = a run of rank r's fp32 shard of parameter p, cast to bf16 into
 // its slot gathered[r*S + o_p + ...].  Per 8 elements: two 16-byte loads,
-// one 16-byte store.
-template <int THREADS>
+// one 16-byte store.  WORKERS as in ag_kernel.
+template <int THREADS, int WORKERS>
 __global__ void __launch_bounds__(THREADS) pack_kernel(PackArgs a) {
-  for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+  constexpr int WT = THREADS / WORKERS;
+  static_assert(THREADS % WORKERS == 0 && WT % 32 == 0, "workers are whole warps");
+  const int lane = (int)threadIdx.x % WT;
+  for (int64_t t = (int64_t)blockIdx.x * WORKERS + (int)threadIdx.x / WT; t < a.num_tiles;
+       t += (int64_t)gridDim.x * WORKERS) {
     const Tile tile = a.tiles[t];
     const float* __restrict__ src = a.stab[(int64_t)tile.r * a.num_params + tile.p] + tile.src;
     uint16_t* __restrict__ dst = a.buf + tile.dst;
     int e0 = 0;
     if (tile.flags & kTileVec) {
       const int nvec = tile.len >> 3;
-      for (int v = threadIdx.x; v < nvec; v += THREADS) {
+      for (int v = lane; v < nvec; v += WT) {
         const uint4 x = ld_stream(src + 8 * v);
         const uint4 y = ld_stream(src + 8 * v + 4);
         uint4 o;
@@ -590,7 +601,7 @@ __global__ void __launch_bounds__(THREADS) pack_kernel(PackArgs a) {
       }
       e0 = 8 * nvec;
     }
-    for (int e = e0 + threadIdx.x; e < tile.len; e += THREADS)
+    for (int e = e0 + lane; e < tile.len; e += WT)
       dst[e] = (uint16_t)f32_to_bf16_bits(src[e]);
   }
 }
@@ -621,10 +632,16 @@ RsKernel rs_kernel_for(int32_t n, bool fat) {
   return fat ? rs_kernel_for<kFatThreads>(n) : rs_kernel_for<kRsThreads>(n);
 }
 
+// capped-mode CTAs: kFatThreads threads as groups of kAgThreads
+constexpr int kFatWorkers = kFatThreads / kAgThreads;
+static_assert(kFatThreads % kAgThreads == 0, "a fat CTA is whole placement groups");
+
 AgKernel ag_kernel_for(bool fat, bool to_buf = false) {
   if (to_buf)
-    return fat ? ag_kernel<kFatThreads, TIDE_AG_UNROLL, true> : ag_kernel<kAgThreads, TIDE_AG_UNROLL, true>;
-  return fat ? ag_kernel<kFatThreads, TIDE_AG_UNROLL, false> : ag_kernel<kAgThreads, TIDE_AG_UNROLL, false>;
+    return fat ? ag_kernel<kFatThreads, kFatWorkers, TIDE_AG_UNROLL, true>
+               : ag_kernel<kAgThreads, 1, TIDE_AG_UNROLL, true>;
+  return fat ? ag_kernel<kFatThreads, kFatWorkers, TIDE_AG_UNROLL, false>
+             : ag_kernel<kAgThreads, 1, TIDE_AG_UNROLL, false>;
 }
 
 }  // namespace
@@ -657,9 +674,9 @@ cudaError_t launch_stage(const AgArgs& a, int grid, bool fat, cudaStream_t strea
 cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
   if (fat)
-    pack_kernel<kFatThreads><<<grid, kFatThreads, 0, stream>>>(a);
+    pack_kernel<kFatThreads, kFatWorkers><<<grid, kFatThreads, 0, stream>>>(a);
   else
-    pack_kernel<kAgThreads><<<grid, kAgThreads, 0, stream>>>(a);
+    pack_kernel<kAgThreads, 1><<<grid, kAgThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -696,7 +713,7 @@ cudaError_t launch_rs_bulk(const RsArgs& a, int grid, cudaStream_t stream) {
 }
 
 cudaError_t pk_occupancy(int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pack_kernel<kAgThreads>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pack_kernel<kAgThreads, 1>,
                                                        kAgThreads, 0);
 }
 

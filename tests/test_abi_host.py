@@ -304,13 +304,16 @@ def test_environment_overrides(monkeypatch):
 
 
 def test_small_layouts_spread_over_the_gpu():
-    """A small layout gets tiles small enough to fill ~1216 CTA slots; a
-    large one keeps the full-size tiles."""
+    """A small layout gets tiles of one CTA pass (4096 elements: 512 threads
+    x 8), at least one per SM of a 152-SM GPU; a large one keeps the
+    full-size tiles."""
     import synth
 
     with tide.Layout(synth.tiny().shapes, 4) as lay:
         for op in (tide.TIDE_OP_RS, tide.TIDE_OP_AG, tide.TIDE_OP_PACK):
-            assert len(lay.tiles(op)) >= 300
+            t = lay.tiles(op)
+            assert len(t) >= 152
+            assert t[:, 4].max() == 4096
     with tide.Layout([(8192, 8192)], 8) as lay:
         t = lay.tiles(tide.TIDE_OP_RS)
         assert t[:, 4].max() == 16384  # 256 KiB of bf16 reads over 8 ranks

@@ -96,13 +96,15 @@ typedef enum {
 } tide_status_t;
 
 typedef enum {
-  /* Kernels launched over the whole GPU (grid sized by occupancy x SMs). */
+  /* Kernels launched over the whole GPU: one CTA per tile of the layout's
+   * work list, handed out in list order by the block scheduler. */
   TIDE_MODE_UNCAPPED = 0,
   /* Persistent kernels with at most `cta_cap` CTAs looping over the tile
    * list: the short-lived-CTA budget of "TIDE的设计思路", trading bandwidth
    * for SM time left to concurrent compute.  Each CTA is 1024 threads wide
    * (an SM hosting one is lost to full-SM compute kernels anyway, so it
-   * keeps a whole SM's loads in flight). */
+   * keeps a whole SM's loads in flight); in the placement, staging and pack
+   * it is two 512-thread groups, each walking its own tiles. */
   TIDE_MODE_CAPPED = 1,
   /* Placement and Slot-Reuse staging through the copy engines
    * (cudaMemcpy2DAsync, no SM use), the copy-engine path of "TIDE的设计思路".

@@ -354,6 +354,30 @@ def test_zero_copy_host_buffers(tiny_job):
     gpu_checks.full_check_ag(job)
 
 
+def test_launch_shapes(tiny_job):
+    """Uncapped: one CTA of 512 threads per tile of each list.  Capped: `cap`
+    CTAs of 1024 threads (fewer if the list is shorter).  Copy engine: no
+    kernel for placement.  Bulk: 32-thread placement CTAs."""
+    lay = tiny_job.layout
+    ops = (tide.TIDE_OP_RS, tide.TIDE_OP_AG, tide.TIDE_OP_PACK, tide.TIDE_OP_STAGE,
+           tide.TIDE_OP_STAGED_RS)
+    for op in ops:
+        n = len(lay.tiles(op))
+        assert n > 16
+        assert lay.launch_shape(op) == (n, 512), op
+    lay.set_mode(tide.TIDE_MODE_CAPPED, 16)
+    for op in ops:
+        assert lay.launch_shape(op) == (16, 1024), op
+    lay.set_mode(tide.TIDE_MODE_CAPPED, 1 << 20)
+    for op in ops:
+        assert lay.launch_shape(op) == (len(lay.tiles(op)), 1024), op
+    lay.set_mode(tide.TIDE_MODE_COPY_ENGINE)
+    assert lay.launch_shape(tide.TIDE_OP_AG)[0] == 0
+    lay.set_mode(tide.TIDE_MODE_BULK)
+    assert lay.launch_shape(tide.TIDE_OP_AG)[1] == 32
+    lay.set_mode(tide.TIDE_MODE_UNCAPPED)
+
+
 def test_bounded_wait_timeout_is_reported(tiny_job):
     """The bulk-copy kernel's waits are bounded: with the test hook set, its
     wait on a barrier nothing arrives on runs out after 1 ms, the kernel

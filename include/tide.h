@@ -323,7 +323,8 @@ TIDE_API tide_status_t tide_rs_staged_bf16_to_fp32(tide_layout_t layout, const u
  * never does, so together with the host-only tide_layout_create a caller can
  * run the reduce-scatter without any allocation.
  *
- * Same arguments, result (bit for bit) and modes as tide_rs_bf16_to_fp32.
+ * Same arguments, result (bit for bit) and modes as tide_rs_bf16_to_fp32
+ * (in TIDE_MODE_BULK it runs the load/store kernel, one CTA per tile).
  * The kernel's scratch (the layout's tile list, 32 bytes per tile, plus
  * 2*N*P device pointers) is copied on `stream` into one file-scope device
  * array of TIDE_NOALLOC_SCRATCH_BYTES (4 MiB) that every GPU loading the

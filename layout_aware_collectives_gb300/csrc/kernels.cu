@@ -714,19 +714,5 @@ cudaError_t launch_rs_bulk(const RsArgs& a, int grid, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t pk_occupancy(int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pack_kernel<kAgThreads, 1>,
-                                                       kAgThreads, 0);
-}
-
-cudaError_t rs_occupancy(int32_t num_ranks, int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, rs_kernel_for(num_ranks, false),
-                                                       kRsThreads, rs_smem_bytes(num_ranks));
-}
-
-cudaError_t ag_occupancy(int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, ag_kernel_for(false),
-                                                       kAgThreads, 0);
-}
 
 }  // namespace tide

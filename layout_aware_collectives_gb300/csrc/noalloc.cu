@@ -94,15 +94,10 @@ extern "C" TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t l,
   tide_status_t st = scratch_for_current_device(&scratch);
   if (st != TIDE_OK) return st;
 
-  int dev = 0, sms = 0, occ = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = rs_occupancy(N, &occ);
-  if (e != cudaSuccess) return cuda_fail(e, "device query");
   const int64_t tiles = (int64_t)l->rs_tiles.size();
-  // the load/store kernel in every mode but capped (one CTA per tile there)
+  // the load/store kernel in every mode: `cap` CTAs when capped, else one per tile
   const tide_mode_t mode = l->mode == TIDE_MODE_CAPPED ? TIDE_MODE_CAPPED : TIDE_MODE_UNCAPPED;
-  const int grid = grid_for(tiles, mode, l->cta_cap, sms, std::max(1, occ));
+  const int grid = grid_for(tiles, mode, l->cta_cap, 0, 0);
 
   // Scratch layout: [tile list][param-major gradient table][rank-major shard table].
   std::vector<const void*> table(2 * (size_t)N * P);
@@ -112,7 +107,7 @@ extern "C" TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t l,
   unsigned char* base = (unsigned char*)scratch;
   // Pageable sources: each copy returns once the driver holds its own copy of
   // the bytes, so the host vectors may go out of scope after the calls.
-  e = cudaMemcpyAsync(base, l->rs_tiles.data(), tile_bytes, cudaMemcpyHostToDevice, stream);
+  cudaError_t e = cudaMemcpyAsync(base, l->rs_tiles.data(), tile_bytes, cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(base + tile_bytes, table.data(), table_bytes, cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return cuda_fail(e, "copy of the tables into the no-allocation scratch");

@@ -18,7 +18,7 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
   } while (0)
 
 struct DeviceShape {
-  int sms = 0, rs_occ = 0, ag_occ = 0, pk_occ = 0, bulk_occ = 0;
+  int sms = 0, bulk_occ = 0;
 };
 
 tide_status_t query_device(const tide_layout_s* l, DeviceShape* d) {
@@ -26,13 +26,7 @@ tide_status_t query_device(const tide_layout_s* l, DeviceShape* d) {
   TIDE_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
   TIDE_CUDA(cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, dev),
             "cudaDeviceGetAttribute(MultiProcessorCount)");
-  TIDE_CUDA(rs_occupancy(l->num_ranks, &d->rs_occ), "occupancy of the reduce-scatter kernel");
-  TIDE_CUDA(ag_occupancy(&d->ag_occ), "occupancy of the placement kernel");
-  TIDE_CUDA(pk_occupancy(&d->pk_occ), "occupancy of the pack kernel");
   TIDE_CUDA(ag_bulk_occupancy(&d->bulk_occ), "occupancy of the bulk-copy kernel");
-  d->rs_occ = std::max(1, d->rs_occ);
-  d->ag_occ = std::max(1, d->ag_occ);
-  d->pk_occ = std::max(1, d->pk_occ);
   d->bulk_occ = std::max(1, d->bulk_occ);
   return TIDE_OK;
 }
@@ -40,15 +34,16 @@ tide_status_t query_device(const tide_layout_s* l, DeviceShape* d) {
 }  // namespace
 
 // Grid of one launch over `tiles` tiles.  Capped modes launch `cap` CTAs
-// that loop over the list; the bulk kernels (every SM) one CTA per resident
-// slot.  The uncapped load/store kernels launch one CTA per tile, so the
-// hardware block scheduler hands tiles out in list order as CTAs retire;
-// on GB300 that streams 3-11% faster than occupancy x SMs CTAs looping over
-// the list (the loop stays: a grid below `tiles` is still correct).
-int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int occ) {
+// that loop over the list.  Otherwise the TMA bulk kernels (bulk_occ > 0,
+// resident CTAs per SM) fill every SM once, and the load/store kernels
+// (bulk_occ = 0) launch one CTA per tile, so the hardware block scheduler
+// hands tiles out in list order as CTAs retire; on GB300 that streams 3-11%
+// faster than occupancy x SMs CTAs looping over the list (the loop stays: a
+// grid below `tiles` is still correct).
+int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int bulk_occ) {
   if (tiles <= 0) return 0;
   const bool capped = mode == TIDE_MODE_CAPPED || (mode == TIDE_MODE_BULK && cap > 0);
-  const int64_t g = capped ? (int64_t)cap : mode == TIDE_MODE_BULK ? (int64_t)sms * occ : tiles;
+  const int64_t g = capped ? (int64_t)cap : bulk_occ > 0 ? (int64_t)sms * bulk_occ : tiles;
   return (int)std::min<int64_t>(std::min<int64_t>(tiles, g), INT32_MAX);
 }
 
@@ -136,9 +131,6 @@ tide_status_t bind_device(tide_layout_s* l, int dev) {
     TIDE_CUDA(cudaEventCreateWithFlags(&s.use_ev, cudaEventDisableTiming), "cudaEventCreate");
   }
   l->num_sms = d.sms;
-  l->rs_occ = d.rs_occ;
-  l->ag_occ = d.ag_occ;
-  l->pk_occ = d.pk_occ;
   l->bulk_occ = d.bulk_occ;
   l->device = dev;
   return TIDE_OK;
@@ -330,8 +322,8 @@ tide_status_t copy_engine(tide_layout_s* l, uint16_t* buf, uint16_t* const* para
 
 }  // namespace
 
-int grid_of(const tide_layout_s* l, int64_t tiles, int occ) {
-  return grid_for(tiles, l->mode, l->cta_cap, l->num_sms, occ);
+int grid_of(const tide_layout_s* l, int64_t tiles, int bulk_occ) {
+  return grid_for(tiles, l->mode, l->cta_cap, l->num_sms, bulk_occ);
 }
 
 }  // namespace tide
@@ -369,7 +361,7 @@ tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, cons
   // measured on GB300: 4 KiB rank slices over every SM, 8 KiB when capped
   a.stage_bytes = l->cta_cap > 0 ? 65536 : 32768;
   cudaError_t e = rs_uses_bulk(l) ? launch_rs_bulk(a, grid_of(l, t1 - t0, 1), stream)
-                                  : launch_rs(a, grid_of(l, t1 - t0, l->rs_occ), l->mode == TIDE_MODE_CAPPED,
+                                  : launch_rs(a, grid_of(l, t1 - t0, 0), l->mode == TIDE_MODE_CAPPED,
                                               stream);
   if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter kernel launch");
   return mark_used(l, slot, stream);
@@ -418,8 +410,8 @@ cudaError_t launch_copy(tide_layout_s* l, AgArgs& a, bool to_buf, cudaStream_t s
   const bool capped = l->mode == TIDE_MODE_CAPPED;
   if (l->mode == TIDE_MODE_BULK)
     return launch_ag_bulk(a, grid_of(l, a.num_tiles, l->bulk_occ), to_buf, stream);
-  return to_buf ? launch_stage(a, grid_of(l, a.num_tiles, l->ag_occ), capped, stream)
-                : launch_ag(a, grid_of(l, a.num_tiles, l->ag_occ), capped, stream);
+  return to_buf ? launch_stage(a, grid_of(l, a.num_tiles, 0), capped, stream)
+                : launch_ag(a, grid_of(l, a.num_tiles, 0), capped, stream);
 }
 
 }  // namespace
@@ -454,7 +446,7 @@ tide_status_t tide_layout_launch_shape(tide_layout_t l, tide_op_t op, int32_t* g
                                                   : (int64_t)l->ag_tiles.size();
   const bool bulk = l->mode == TIDE_MODE_BULK && (op == TIDE_OP_AG || op == TIDE_OP_STAGE);
   const bool rs_bulk = rs_like && rs_uses_bulk(l);
-  const int occ = rs_bulk ? 1 : rs_like ? d.rs_occ : op == TIDE_OP_PACK ? d.pk_occ : bulk ? d.bulk_occ : d.ag_occ;
+  const int occ = rs_bulk ? 1 : bulk ? d.bulk_occ : 0;
   *grid = l->mode == TIDE_MODE_COPY_ENGINE ? 0 : grid_for(tiles, l->mode, l->cta_cap, d.sms, occ);
   *block = rs_bulk ? kRsBulkThreads : rs_like ? rs_block(capped) : op == TIDE_OP_PACK ? pk_block(capped)
                    : bulk ? 32 : ag_block(capped);
@@ -578,7 +570,7 @@ tide_status_t tide_ag_pack_bf16(tide_layout_t l, int32_t rank, const float* cons
   a.stab = (const float* const*)slot->d_table;
   a.buf = gathered;
   a.num_params = P;
-  cudaError_t e = launch_pack(a, grid_of(l, t1 - t0, l->pk_occ), l->mode == TIDE_MODE_CAPPED, stream);
+  cudaError_t e = launch_pack(a, grid_of(l, t1 - t0, 0), l->mode == TIDE_MODE_CAPPED, stream);
   if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
   return mark_used(l, slot, stream);
 }

@@ -132,9 +132,6 @@ int rs_block(bool fat);
 int ag_block(bool fat);
 int pk_block(bool fat);
 // Resident CTAs per SM of each kernel for `num_ranks` (RS) at its block size.
-cudaError_t rs_occupancy(int32_t num_ranks, int* blocks_per_sm);
-cudaError_t ag_occupancy(int* blocks_per_sm);
-cudaError_t pk_occupancy(int* blocks_per_sm);
 size_t rs_smem_bytes(int32_t num_ranks);
 
 // Device-side pointer table, cached by content.
@@ -182,7 +179,7 @@ struct tide_layout_s {
   tide::Tile* d_pk_tiles = nullptr;
   tide::Tile* d_st_tiles = nullptr;  // RS tiles whose sources are slot offsets
   int num_sms = 0;
-  int rs_occ = 0, ag_occ = 0, pk_occ = 0, bulk_occ = 0;
+  int bulk_occ = 0;  // resident bulk-copy CTAs per SM
   int* d_err = nullptr;         // device error word of the bulk-copy kernels
   int64_t test_stall_ns = 0;    // test hook of the bounded waits
   int max_pitch = 0;
@@ -194,6 +191,6 @@ struct tide_layout_s {
 namespace tide {
 tide_status_t set_error(tide_status_t st, const std::string& msg);
 tide_status_t cuda_fail(cudaError_t e, const char* what);
-int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int occ);
-int grid_of(const tide_layout_s* l, int64_t tiles, int occ);
+int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int bulk_occ);
+int grid_of(const tide_layout_s* l, int64_t tiles, int bulk_occ);
 }  // namespace tide

@@ -470,6 +470,7 @@ def run_next_ops(tide, layout, job, wl, stream, reps=20):
     padded = sum(job.shard_numel)
     outs = [torch.empty(n, dtype=torch.float32, device="cuda") for n in job.shard_numel]
     job.make_pack_inputs()
+    torch.cuda.synchronize()  # the generator fills run on the default stream
     gptr = tide.PointerTable(job.grad_ptrs())
     optr = tide.PointerTable(outs)
     pptr = tide.PointerTable(job.pack_src_ptrs())
@@ -495,6 +496,7 @@ def run_next_ops(tide, layout, job, wl, stream, reps=20):
     # Slot-Reuse two-stage path: stage every rank's gradients into its slot,
     # then reduce-scatter from the slots
     job.make_slots()
+    torch.cuda.synchronize()
     sptr = tide.PointerTable(job.shard_ptrs())
     slot_tab = tide.PointerTable(job.slots)
     gtabs = [tide.PointerTable([job.grads[k][p] for p in range(job.P)]) for k in range(N)]
@@ -597,6 +599,7 @@ def run_stock(job, wl, stream, tide_rs_ms, tide_ag_ms, reps=10):
     import torch
 
     st = StockFSDP2(job)
+    torch.cuda.synchronize()  # set-up work ran on the default stream
     N, psi, padded = wl.num_ranks, wl.psi, sum(job.shard_numel)
     flat = N * padded  # elements of one rank's flat buffer (every destination block)
     parts = {"rs_copy_in": (st.copy_in, N * (2 * psi + 4 * flat)),
@@ -747,6 +750,7 @@ def run_interference(tide, layout, job, wl, props):
     a = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
     b = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
     c = torch.empty(n, n, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()  # the operands are written on the default stream
     sg = torch.cuda.Stream()
     sr = torch.cuda.Stream()
     gptr = tide.PointerTable(job.grad_ptrs())

@@ -296,19 +296,24 @@ def test_full_size_sampled_parity(name):
                 assert torch.equal(job.shards[r][p].view(torch.int32), ref_all[r][p].view(torch.int32))
         del job.slots, ref_all
         ref = [s.clone() for s in (job.shards[0][0], job.shards[-1][-1])]
-        lay.set_mode(tide.TIDE_MODE_CAPPED, 64)
-        for row in job.shards:
-            for s in row:
-                s.fill_(float("nan"))
-        run(job)
-        assert torch.equal(job.shards[0][0], ref[0]) and torch.equal(job.shards[-1][-1], ref[1])
-        gpu_checks.torch_check_rs(job)
-        # TMA bulk-staged reduce-scatter, capped and over every SM
-        for cap in (16, 0):
-            lay.set_mode(tide.TIDE_MODE_BULK, cap)
+
+        def clear_outputs():
             for row in job.shards:
                 for s in row:
                     s.fill_(float("nan"))
+            for prm in job.params:
+                prm.fill_(0x7FA5)  # a bf16 NaN pattern the placement never writes
+
+        lay.set_mode(tide.TIDE_MODE_CAPPED, 64)
+        clear_outputs()
+        run(job)
+        assert torch.equal(job.shards[0][0], ref[0]) and torch.equal(job.shards[-1][-1], ref[1])
+        gpu_checks.torch_check_rs(job)
+        gpu_checks.torch_check_ag(job)
+        # TMA bulk-staged reduce-scatter and bulk-copy placement, capped and over every SM
+        for cap in (16, 0):
+            lay.set_mode(tide.TIDE_MODE_BULK, cap)
+            clear_outputs()
             run(job)
             lay.check_device()
             gpu_checks.torch_check_rs(job)

@@ -358,8 +358,13 @@ tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, cons
   a.err = l->d_err;
   a.timeout_ns = TIDE_BULK_TIMEOUT_NS;
   a.test_stall_ns = (uint64_t)l->test_stall_ns;
-  // measured on GB300: 4 KiB rank slices over every SM, 8 KiB when capped
-  a.stage_bytes = l->cta_cap > 0 ? 65536 : 32768;
+  // TMA-staged kernel: a stage holds one chunk's N rank slices.  Measured on
+  // GB300, slices of 4 KiB over every SM (8 KiB when capped) keep the
+  // bulk-copy engine busy and smaller ones do not, so the stage grows with N
+  // from 32 KiB (64 KiB capped) up to half the 192 KiB ring (two stages).
+  const int64_t slice_target = l->cta_cap > 0 ? 8192 : 4096;
+  a.stage_bytes = (int32_t)std::min<int64_t>(
+      98304, std::max<int64_t>(l->cta_cap > 0 ? 65536 : 32768, (int64_t)l->num_ranks * slice_target));
   cudaError_t e = rs_uses_bulk(l) ? launch_rs_bulk(a, grid_of(l, t1 - t0, 1), stream)
                                   : launch_rs(a, grid_of(l, t1 - t0, 0), l->mode == TIDE_MODE_CAPPED,
                                               stream);

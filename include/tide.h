@@ -116,7 +116,8 @@ typedef enum {
    * -> global copies issued by one lane per CTA.  Reduce-scatter (all three
    * forms, N <= 512; larger N runs the load/store kernel): one 288-thread
    * CTA per SM whose producer warp stages the N rank slices of each chunk
-   * (32 KiB per chunk, 64 KiB when capped) in a 192 KiB shared-memory ring
+   * (4 KiB per slice, 8 KiB when capped; 32 KiB to 96 KiB per chunk, 64 KiB
+   * to 96 KiB when capped) in a 192 KiB shared-memory ring
    * and whose 8 consumer warps sum them.  The pack runs as in
    * TIDE_MODE_UNCAPPED.  cta_cap > 0 caps the grid at cta_cap CTAs (one per
    * SM), cta_cap = 0 uses every SM. */

@@ -693,13 +693,6 @@ cudaError_t launch_ag_bulk(const AgArgs& a, int grid, bool to_buf, cudaStream_t 
   return cudaGetLastError();
 }
 
-cudaError_t ag_bulk_occupancy(int* blocks_per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(ag_bulk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kBulkSmem);
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, ag_bulk_kernel<false>, 32, kBulkSmem);
-}
-
 cudaError_t launch_rs_bulk(const RsArgs& a, int grid, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
   const int N = a.num_ranks;

@@ -18,32 +18,30 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
   } while (0)
 
 struct DeviceShape {
-  int sms = 0, bulk_occ = 0;
+  int sms = 0;
 };
 
-tide_status_t query_device(const tide_layout_s* l, DeviceShape* d) {
+tide_status_t query_device(DeviceShape* d) {
   int dev = 0;
   TIDE_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
   TIDE_CUDA(cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, dev),
             "cudaDeviceGetAttribute(MultiProcessorCount)");
-  TIDE_CUDA(ag_bulk_occupancy(&d->bulk_occ), "occupancy of the bulk-copy kernel");
-  d->bulk_occ = std::max(1, d->bulk_occ);
   return TIDE_OK;
 }
 
 }  // namespace
 
 // Grid of one launch over `tiles` tiles.  Capped modes launch `cap` CTAs
-// that loop over the list.  Otherwise the TMA bulk kernels (bulk_occ > 0,
-// resident CTAs per SM) fill every SM once, and the load/store kernels
-// (bulk_occ = 0) launch one CTA per tile, so the hardware block scheduler
-// hands tiles out in list order as CTAs retire; on GB300 that streams 3-11%
-// faster than occupancy x SMs CTAs looping over the list (the loop stays: a
-// grid below `tiles` is still correct).
-int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int bulk_occ) {
+// that loop over the list.  Otherwise the TMA-staged reduce-scatter
+// (per_sm > 0: its ring fills an SM) launches per_sm CTAs per SM, and every
+// other kernel one CTA per tile, so the hardware block scheduler hands tiles
+// out in list order as CTAs retire; on GB300 that streams 3-17% faster than
+// SM-filling CTAs looping over the list (the loop stays: a grid below
+// `tiles` is still correct).
+int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int per_sm) {
   if (tiles <= 0) return 0;
   const bool capped = mode == TIDE_MODE_CAPPED || (mode == TIDE_MODE_BULK && cap > 0);
-  const int64_t g = capped ? (int64_t)cap : bulk_occ > 0 ? (int64_t)sms * bulk_occ : tiles;
+  const int64_t g = capped ? (int64_t)cap : per_sm > 0 ? (int64_t)sms * per_sm : tiles;
   return (int)std::min<int64_t>(std::min<int64_t>(tiles, g), INT32_MAX);
 }
 
@@ -85,8 +83,8 @@ void release_device(tide_layout_s* l) {
 
 tide_status_t bind_device(tide_layout_s* l, int dev);
 
-// Bind the layout to the current device on first use: query the SM count
-// and occupancy, upload the tile lists.  On failure everything allocated so
+// Bind the layout to the current device on first use: query the SM count,
+// upload the tile lists.  On failure everything allocated so
 // far is released and the layout stays unbound.
 tide_status_t ensure_device(tide_layout_s* l) {
   int dev = 0;
@@ -104,7 +102,7 @@ tide_status_t ensure_device(tide_layout_s* l) {
 
 tide_status_t bind_device(tide_layout_s* l, int dev) {
   DeviceShape d;
-  tide_status_t st = query_device(l, &d);
+  tide_status_t st = query_device(&d);
   if (st != TIDE_OK) return st;
   TIDE_CUDA(cudaDeviceGetAttribute(&l->max_pitch, cudaDevAttrMaxPitch, dev),
             "cudaDeviceGetAttribute(MaxPitch)");
@@ -131,7 +129,6 @@ tide_status_t bind_device(tide_layout_s* l, int dev) {
     TIDE_CUDA(cudaEventCreateWithFlags(&s.use_ev, cudaEventDisableTiming), "cudaEventCreate");
   }
   l->num_sms = d.sms;
-  l->bulk_occ = d.bulk_occ;
   l->device = dev;
   return TIDE_OK;
 }
@@ -322,8 +319,8 @@ tide_status_t copy_engine(tide_layout_s* l, uint16_t* buf, uint16_t* const* para
 
 }  // namespace
 
-int grid_of(const tide_layout_s* l, int64_t tiles, int bulk_occ) {
-  return grid_for(tiles, l->mode, l->cta_cap, l->num_sms, bulk_occ);
+int grid_of(const tide_layout_s* l, int64_t tiles, int per_sm) {
+  return grid_for(tiles, l->mode, l->cta_cap, l->num_sms, per_sm);
 }
 
 }  // namespace tide
@@ -414,7 +411,7 @@ cudaError_t launch_copy(tide_layout_s* l, AgArgs& a, bool to_buf, cudaStream_t s
   a.test_stall_ns = (uint64_t)l->test_stall_ns;
   const bool capped = l->mode == TIDE_MODE_CAPPED;
   if (l->mode == TIDE_MODE_BULK)
-    return launch_ag_bulk(a, grid_of(l, a.num_tiles, l->bulk_occ), to_buf, stream);
+    return launch_ag_bulk(a, grid_of(l, a.num_tiles, 0), to_buf, stream);
   return to_buf ? launch_stage(a, grid_of(l, a.num_tiles, 0), capped, stream)
                 : launch_ag(a, grid_of(l, a.num_tiles, 0), capped, stream);
 }
@@ -441,7 +438,7 @@ tide_status_t tide_layout_launch_shape(tide_layout_t l, tide_op_t op, int32_t* g
   if (op < TIDE_OP_RS || op > TIDE_OP_STAGED_RS) return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
   std::lock_guard<std::mutex> g(l->mu);
   DeviceShape d;
-  tide_status_t st = query_device(l, &d);
+  tide_status_t st = query_device(&d);
   if (st != TIDE_OK) return st;
   const bool capped = l->mode == TIDE_MODE_CAPPED;
   const bool rs_like = op == TIDE_OP_RS || op == TIDE_OP_STAGED_RS;
@@ -451,8 +448,8 @@ tide_status_t tide_layout_launch_shape(tide_layout_t l, tide_op_t op, int32_t* g
                                                   : (int64_t)l->ag_tiles.size();
   const bool bulk = l->mode == TIDE_MODE_BULK && (op == TIDE_OP_AG || op == TIDE_OP_STAGE);
   const bool rs_bulk = rs_like && rs_uses_bulk(l);
-  const int occ = rs_bulk ? 1 : bulk ? d.bulk_occ : 0;
-  *grid = l->mode == TIDE_MODE_COPY_ENGINE ? 0 : grid_for(tiles, l->mode, l->cta_cap, d.sms, occ);
+  const int per_sm = rs_bulk ? 1 : 0;
+  *grid = l->mode == TIDE_MODE_COPY_ENGINE ? 0 : grid_for(tiles, l->mode, l->cta_cap, d.sms, per_sm);
   *block = rs_bulk ? kRsBulkThreads : rs_like ? rs_block(capped) : op == TIDE_OP_PACK ? pk_block(capped)
                    : bulk ? 32 : ag_block(capped);
   return TIDE_OK;

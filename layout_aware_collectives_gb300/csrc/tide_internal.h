@@ -121,7 +121,6 @@ cudaError_t launch_stage(const AgArgs& a, int grid, bool fat, cudaStream_t strea
 // Bulk-copy (TMA engine) placement / staging: one issuing lane per CTA,
 // shared-memory ring of TIDE_BULK_STAGES x TIDE_BULK_CHUNK bytes.
 cudaError_t launch_ag_bulk(const AgArgs& a, int grid, bool to_buf, cudaStream_t stream);
-cudaError_t ag_bulk_occupancy(int* blocks_per_sm);
 // Bulk-staged reduce-scatter (TMA engine): one CTA per SM, rank slices staged
 // in shared memory by a producer warp; N <= kRsBulkMaxRanks.
 constexpr int kRsBulkMaxRanks = 1024;  // bulk RS runs for N <= kRsBulkMaxRanks / 2
@@ -179,7 +178,6 @@ struct tide_layout_s {
   tide::Tile* d_pk_tiles = nullptr;
   tide::Tile* d_st_tiles = nullptr;  // RS tiles whose sources are slot offsets
   int num_sms = 0;
-  int bulk_occ = 0;  // resident bulk-copy CTAs per SM
   int* d_err = nullptr;         // device error word of the bulk-copy kernels
   int64_t test_stall_ns = 0;    // test hook of the bounded waits
   int max_pitch = 0;
@@ -191,6 +189,6 @@ struct tide_layout_s {
 namespace tide {
 tide_status_t set_error(tide_status_t st, const std::string& msg);
 tide_status_t cuda_fail(cudaError_t e, const char* what);
-int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int bulk_occ);
-int grid_of(const tide_layout_s* l, int64_t tiles, int bulk_occ);
+int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int per_sm);
+int grid_of(const tide_layout_s* l, int64_t tiles, int per_sm);
 }  // namespace tide

@@ -362,7 +362,8 @@ def test_zero_copy_host_buffers(tiny_job):
 def test_launch_shapes(tiny_job):
     """Uncapped: one CTA of 512 threads per tile of each list.  Capped: `cap`
     CTAs of 1024 threads (fewer if the list is shorter).  Copy engine: no
-    kernel for placement.  Bulk: 32-thread placement CTAs."""
+    kernel for placement.  Bulk: one 32-thread placement CTA per tile and
+    one 288-thread reduce-scatter CTA per SM, or `cap` of either."""
     lay = tiny_job.layout
     ops = (tide.TIDE_OP_RS, tide.TIDE_OP_AG, tide.TIDE_OP_PACK, tide.TIDE_OP_STAGE,
            tide.TIDE_OP_STAGED_RS)
@@ -379,7 +380,12 @@ def test_launch_shapes(tiny_job):
     lay.set_mode(tide.TIDE_MODE_COPY_ENGINE)
     assert lay.launch_shape(tide.TIDE_OP_AG)[0] == 0
     lay.set_mode(tide.TIDE_MODE_BULK)
-    assert lay.launch_shape(tide.TIDE_OP_AG)[1] == 32
+    assert lay.launch_shape(tide.TIDE_OP_AG) == (len(lay.tiles(tide.TIDE_OP_AG)), 32)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert lay.launch_shape(tide.TIDE_OP_RS) == (min(sms, len(lay.tiles(tide.TIDE_OP_RS))), 288)
+    lay.set_mode(tide.TIDE_MODE_BULK, 3)
+    assert lay.launch_shape(tide.TIDE_OP_AG) == (3, 32)
+    assert lay.launch_shape(tide.TIDE_OP_RS) == (3, 288)
     lay.set_mode(tide.TIDE_MODE_UNCAPPED)
 
 

@@ -743,7 +743,11 @@ def run_e2e(tide, layout, job, wl, stream, K, world):
 
 def run_interference(tide, layout, job, wl, props):
     """Slowdown of a bf16 8192^3 GEMM on one stream while the reduce-scatter
-    (or placement) loops on another, per mode; SM.time of each mode."""
+    (or placement) loops on another, per mode; the op's bandwidth during the
+    GEMM window and its SM.time.  Modes marked `_lowprio` put the GEMM on a
+    high-priority stream and the op on a low-priority one: the block
+    scheduler then dispatches pending GEMM CTAs first, and the op's
+    one-CTA-per-tile launches fill whatever the GEMM leaves."""
     import torch
 
     n = 8192
@@ -751,14 +755,15 @@ def run_interference(tide, layout, job, wl, props):
     b = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
     c = torch.empty(n, n, dtype=torch.bfloat16, device="cuda")
     torch.cuda.synchronize()  # the operands are written on the default stream
-    sg = torch.cuda.Stream()
-    sr = torch.cuda.Stream()
+    least, greatest = torch.cuda.Stream.priority_range()
+    streams = {False: (torch.cuda.Stream(), torch.cuda.Stream()),
+               True: (torch.cuda.Stream(priority=greatest), torch.cuda.Stream(priority=least))}
     gptr = tide.PointerTable(job.grad_ptrs())
     sptr = tide.PointerTable(job.shard_ptrs())
     pptr = tide.PointerTable(job.param_ptrs())
     reps = 8
 
-    def gemm_ms():
+    def gemm_events(sg):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(sg):
             e0.record(sg)
@@ -767,37 +772,39 @@ def run_interference(tide, layout, job, wl, props):
             e1.record(sg)
         return e0, e1
 
-    def op_ms(op, count=3):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(sr)
-        for _ in range(count):
-            op()
-        e1.record(sr)
+    def gemm_alone(sg):
+        for _ in range(3):
+            gemm_events(sg)
         torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / count
+        t = []
+        for _ in range(5):
+            e0, e1 = gemm_events(sg)
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1) / reps)
+        return statistics.median(t)
 
-    # GEMM alone
-    for _ in range(3):
-        gemm_ms()
-    torch.cuda.synchronize()
-    alone = []
-    for _ in range(5):
-        e0, e1 = gemm_ms()
-        torch.cuda.synchronize()
-        alone.append(e0.elapsed_time(e1) / reps)
-    t0 = statistics.median(alone)
+    t0 = gemm_alone(streams[False][0])
+    t0_hi = gemm_alone(streams[True][0])
     flops = 2 * n ** 3
     res = {"gemm": f"bf16 {n}x{n}x{n} torch.matmul", "gemm_ms_alone": round(t0, 4),
-           "gemm_tflops_alone": round(flops / (t0 * 1e-3) / 1e12, 1), "modes": []}
-    modes = [("rs", "uncapped", tide.TIDE_MODE_UNCAPPED, 0)]
-    modes += [("rs", f"capped{cap}", tide.TIDE_MODE_CAPPED, cap) for cap in (8, 16, 32, 64)]
-    modes += [("rs", f"bulk_tma_capped{cap}", tide.TIDE_MODE_BULK, cap) for cap in (8, 16, 32, 64)]
-    modes += [("rs", "bulk_tma_uncapped", tide.TIDE_MODE_BULK, 0)]
-    modes += [("ag", "uncapped", tide.TIDE_MODE_UNCAPPED, 0),
-              ("ag", "bulk_tma", tide.TIDE_MODE_BULK, 0),
-              ("ag", "capped16", tide.TIDE_MODE_CAPPED, 16),
-              ("ag", "copy_engine", tide.TIDE_MODE_COPY_ENGINE, 0)]
-    for kind, name, mode, cap in modes:
+           "gemm_tflops_alone": round(flops / (t0 * 1e-3) / 1e12, 1),
+           "gemm_ms_alone_high_priority": round(t0_hi, 4),
+           "stream_priorities": {"least": least, "greatest": greatest},
+           "op_GB/s_during_gemm": "bytes the op moved inside the GEMM window (each launch weighted by "
+                                  "its overlap with the window) / window length",
+           "modes": []}
+    U, C, B, CE = (tide.TIDE_MODE_UNCAPPED, tide.TIDE_MODE_CAPPED, tide.TIDE_MODE_BULK,
+                   tide.TIDE_MODE_COPY_ENGINE)
+    modes = [("rs", "uncapped", U, 0, False), ("rs", "uncapped_lowprio", U, 0, True)]
+    modes += [("rs", f"capped{cap}", C, cap, False) for cap in (8, 16, 32, 64)]
+    modes += [("rs", f"bulk_tma_capped{cap}", B, cap, False) for cap in (8, 16, 32, 64)]
+    modes += [("rs", "bulk_tma_uncapped", B, 0, False), ("rs", "bulk_tma_uncapped_lowprio", B, 0, True)]
+    modes += [("ag", "uncapped", U, 0, False), ("ag", "uncapped_lowprio", U, 0, True),
+              ("ag", "bulk_tma", B, 0, False), ("ag", "bulk_tma_lowprio", B, 0, True),
+              ("ag", "capped16", C, 16, False), ("ag", "copy_engine", CE, 0, False)]
+    for kind, name, mode, cap, prio in modes:
+        sg, sr = streams[prio]
+        base = t0_hi if prio else t0
         layout.set_mode(mode, cap)
         if kind == "rs":
             def op():
@@ -811,32 +818,49 @@ def run_interference(tide, layout, job, wl, props):
             opname = tide.TIDE_OP_AG
         with torch.cuda.stream(sr):
             op()
-            alone_ms = op_ms(op)
-            # enough launches to cover the GEMM window twice over
-            count = max(2, int(2 * reps * t0 / max(alone_ms, 1e-3)) + 2)
             torch.cuda.synchronize()
-            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s0.record(sr)
-            for _ in range(count):
+            x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            x0.record(sr)
+            for _ in range(3):
                 op()
-            s1.record(sr)
-        # start the GEMMs once the reduce-scatter loop is running
+            x1.record(sr)
+            torch.cuda.synchronize()
+            alone_ms = x0.elapsed_time(x1) / 3
+            # enough launches to cover the GEMM window twice over, one event pair each
+            count = max(2, int(2 * reps * base / max(alone_ms, 1e-3)) + 2)
+            evs = []
+            for _ in range(count):
+                x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                x0.record(sr)
+                op()
+                x1.record(sr)
+                evs.append((x0, x1))
+        # start the GEMMs once the op loop is running
         time.sleep(0.002)
-        e0, e1 = gemm_ms()
+        e0, e1 = gemm_events(sg)
         torch.cuda.synchronize()
-        t1 = e0.elapsed_time(e1) / reps
-        loop_ms = s0.elapsed_time(s1) / count
+        window = e0.elapsed_time(e1)
+        t1 = window / reps
+        moved = 0.0
+        for x0, x1 in evs:
+            st, en = e0.elapsed_time(x0), e0.elapsed_time(x1)
+            if en > st:
+                moved += nbytes * max(0.0, min(en, window) - max(st, 0.0)) / (en - st)
+        loop_ms = evs[0][0].elapsed_time(evs[-1][1]) / count
         grid, _ = layout.launch_shape(opname)
         sm_used = min(grid, props.multi_processor_count) if grid else 0
         res["modes"].append({
             "op": kind, "mode": name, "grid": grid,
+            "priority": "gemm high, op low" if prio else "equal",
             "op_ms_alone": round(alone_ms, 4),
             "op_GB/s_alone": round(nbytes / (alone_ms * 1e-3) / 1e9, 1),
             "op_ms_concurrent": round(loop_ms, 4),
+            "op_GB/s_during_gemm": round(moved / (window * 1e-3) / 1e9, 1),
             "gemm_ms_concurrent": round(t1, 4),
-            "gemm_slowdown_pct": round(100.0 * (t1 / t0 - 1.0), 2),
+            "gemm_slowdown_pct": round(100.0 * (t1 / base - 1.0), 2),
             "sm_ms": round(alone_ms * sm_used, 2),
         })
+    layout.set_mode(tide.TIDE_MODE_UNCAPPED, 0)
     del a, b, c
     return res
 

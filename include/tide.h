@@ -56,6 +56,13 @@
  *    the layout only once such graphs are no longer replayed.
  *  - A failed CUDA call is reported through the status and cleared from the
  *    runtime's per-thread last error.
+ *  - Next to compute kernels, enqueue the calls on a low-priority stream
+ *    (cudaStreamCreateWithPriority) and the compute on a higher-priority
+ *    one: outside the capped mode every launch is one short-lived CTA per
+ *    tile, so the block scheduler dispatches the compute kernel's pending
+ *    CTAs first and the collective fills what it leaves (on GB300 a bf16
+ *    8192^3 GEMM then runs at its solo speed while the reduce-scatter still
+ *    moves ~2.4 TB/s beside it).
  *  - A layout may be used from several host threads (calls are serialised
  *    internally).  Calls on different streams that write the same output
  *    buffers race, as any two kernels would.

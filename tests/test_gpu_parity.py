@@ -106,6 +106,31 @@ def test_other_stream(tiny_job):
     gpu_checks.full_check_ag(job)
 
 
+@pytest.mark.parametrize("mode", MODES[:2] + [("bulk", tide.TIDE_MODE_BULK, 0)], ids=lambda m: m[0])
+def test_low_priority_stream_next_to_gemm(tiny_job, mode):
+    """The step on a low-priority stream while bf16 GEMMs run on a
+    high-priority one (the arrangement that keeps the GEMM's slowdown small):
+    same bits as the oracle."""
+    job = tiny_job
+    job.layout.set_mode(*mode[1:])
+    least, greatest = torch.cuda.Stream.priority_range()
+    s_lo = torch.cuda.Stream(priority=least)
+    s_hi = torch.cuda.Stream(priority=greatest)
+    a = torch.randn(2048, 2048, dtype=torch.bfloat16, device="cuda")
+    c = torch.empty_like(a)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s_hi):
+        for _ in range(4):
+            torch.matmul(a, a, out=c)
+    for _ in range(3):
+        job.layout.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), job.wl.scale, stream=s_lo)
+        job.layout.place(job.gathered, job.param_ptrs(), stream=s_lo)
+    torch.cuda.synchronize()
+    job.layout.check_device()
+    gpu_checks.full_check_rs(job)
+    gpu_checks.full_check_ag(job)
+
+
 def _ragged_cases():
     rng = np.random.default_rng(11)
     cases = []

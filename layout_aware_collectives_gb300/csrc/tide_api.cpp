@@ -48,7 +48,8 @@ int grid_for(int64_t tiles, tide_mode_t mode, int32_t cap, int sms, int per_sm) 
 namespace {
 
 bool rs_uses_bulk(const tide_layout_s* l) {
-  // slices of at least 8 elements within a 64 KiB stage
+  // N <= 512 keeps rank slices of at least 96 elements in a 96 KiB stage and
+  // the N source pointers within the CTA's shared memory
   return l->mode == TIDE_MODE_BULK && l->num_ranks <= kRsBulkMaxRanks / 2;
 }
 

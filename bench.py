@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "RS / AG-placement HBM GB/s and % of GB300 peak; concurrent GEMM slowdown %"
-L2_BYTES = 129 * 1024 * 1024
+L2_BYTES = 129 * 1024 * 1024  # GB300; used when the device does not report its L2 size
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
 KERNEL_SRC = os.path.join(ROOT, "layout_aware_collectives_gb300", "csrc", "kernels.cu")
@@ -346,8 +346,9 @@ def run_tide(args):
     pptr = tide.PointerTable(job.param_ptrs())
     scale = wl.scale
     rs_bytes, ag_bytes = wl.rs_bytes(), wl.ag_bytes()
-    small = (rs_bytes + ag_bytes) < 2 * L2_BYTES
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if small else None
+    l2_bytes = getattr(props, "L2_cache_size", 0) or L2_BYTES  # queried; the constant if unknown
+    small = (rs_bytes + ag_bytes) < 2 * l2_bytes
+    flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device="cuda") if small else None
 
     step_mode = {"uncapped": tide.TIDE_MODE_UNCAPPED, "capped": tide.TIDE_MODE_CAPPED,
                  "bulk": tide.TIDE_MODE_BULK}[args.mode]

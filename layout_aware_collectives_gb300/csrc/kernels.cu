@@ -655,7 +655,13 @@ int ag_block(bool fat) { return fat ? kFatThreads : kAgThreads; }
 
 cudaError_t launch_rs(const RsArgs& a, int grid, bool fat, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
-  rs_kernel_for(a.num_ranks, fat)<<<grid, rs_block(fat), rs_smem_bytes(a.num_ranks), stream>>>(a);
+  const RsKernel k = rs_kernel_for(a.num_ranks, fat);
+  const size_t smem = rs_smem_bytes(a.num_ranks);
+  if (smem > 48 * 1024) {  // 2*N staged pointers: above 3072 ranks they need the opt-in size
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  k<<<grid, rs_block(fat), smem, stream>>>(a);
   return cudaGetLastError();
 }
 

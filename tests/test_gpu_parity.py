@@ -360,6 +360,27 @@ def test_int64_offsets():
         torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("mode", [MODES[0], MODES[1], ("bulk", tide.TIDE_MODE_BULK, 0)], ids=lambda m: m[0])
+def test_max_ranks(mode):
+    """N = 4096, the most ranks a layout takes: the runtime-N reduce-scatter
+    stages 2*N source pointers in 64 KiB of shared memory (above the 48 KiB
+    launch default), most ranks own padding only, and the bulk mode falls
+    back to the load/store kernel above 512 ranks.  Every element against
+    the oracle, guard bands intact."""
+    n = 4096
+    wl = synth.custom("max_ranks", n, [(n + 3, 8), (5,), (2 * n, 3)], sigma=1e-2, seed=5)
+    with tide.Layout(wl.shapes, n) as lay:
+        lay.set_mode(*mode[1:])
+        job = DeviceJob(wl, lay)
+        run(job)
+        lay.check_device()
+        gpu_checks.full_check_rs(job)
+        gpu_checks.full_check_ag(job)
+        assert job.guards_intact()
+        del job
+        torch.cuda.empty_cache()
+
+
 def test_zero_copy_host_buffers(tiny_job):
     """Inputs and outputs in pinned host memory, read and written by the
     kernels directly: same bits as the oracle."""

@@ -342,10 +342,15 @@ TIDE_API tide_status_t tide_rs_staged_bf16_to_fp32(tide_layout_t layout, const u
  * at zero.  All calls share the array, which keeps the last call's tables:
  * calls that overlap on the GPU (on different streams, or from different
  * layouts without stream ordering between them) race.  The first call on
- * each device looks up the array's device address (cudaGetSymbolAddress);
- * make that first call before any stream capture.  The tables are copied
- * from pageable host memory, so the call returns once the driver has taken
- * its copy of them.  No cudaMalloc, cudaFree or other allocating routine is
+ * each device looks up the array's device address (cudaGetSymbolAddress).
+ * The tables are copied from pageable host memory, so a call that copies
+ * returns only once the stream's earlier work has completed and the driver
+ * has taken its copy of them.  A call on the same stream, with the same
+ * layout and the same pointers as the call that last filled the array,
+ * copies nothing and returns at once (stream order already puts the
+ * earlier copies before its kernel).  Inside a stream capture the call
+ * returns TIDE_ERR_UNSUPPORTED: pageable copies cannot be replayed from a
+ * CUDA graph.  No cudaMalloc, cudaFree or other allocating routine is
  * called.
  */
 TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t layout, const uint16_t* const* grads,

@@ -12,6 +12,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <new>
 
 #include "tide_internal.h"
@@ -142,6 +143,8 @@ tide_status_t create(int32_t num_params, const int32_t* ndims, const int64_t* di
 
   tide_layout_s* l = new (std::nothrow) tide_layout_s();
   if (!l) return set_error(TIDE_ERR_OUT_OF_MEMORY, "host allocation failed");
+  static std::atomic<uint64_t> next_serial{1};
+  l->serial = next_serial.fetch_add(1);
   l->num_ranks = num_ranks;
   l->num_params = num_params;
   l->align = align;

@@ -35,7 +35,21 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
-tide_status_t scratch_for_current_device(void** out) {
+// What each device's array holds: the tile list of layout `serial` and a
+// pointer table, both copied on `stream`.  A later call on the same stream
+// with the same layout and pointers skips the copies, since stream order
+// already puts them before its kernel (a stream handle is only handed out
+// again after the destroyed stream's work has completed).  Guarded by
+// g_held_mu, held from the check through the kernel launch.
+struct Held {
+  uint64_t serial = 0;  // 0: nothing known to be there
+  cudaStream_t stream = nullptr;
+  std::vector<const void*> table;
+};
+std::mutex g_held_mu;
+Held g_held[kMaxDevices];
+
+tide_status_t scratch_for_current_device(void** out, int* dev_out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -49,6 +63,7 @@ tide_status_t scratch_for_current_device(void** out) {
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];
+  *dev_out = dev;
   return TIDE_OK;
 }
 
@@ -90,8 +105,18 @@ extern "C" TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t l,
                      "layout needs " + std::to_string(tile_bytes + table_bytes) +
                          " bytes of scratch (tile list + pointer tables); the no-allocation "
                          "entry point holds at most " + std::to_string(kNoallocScratchBytes));
+  // Pageable copies cannot live in a CUDA graph (the host table is gone at
+  // replay), so a capture is refused before anything is enqueued.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t ce = cudaStreamIsCapturing(stream, &cs);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone)
+    return set_error(TIDE_ERR_UNSUPPORTED,
+                     "the no-allocation entry point copies its tables from pageable host memory "
+                     "and cannot be captured into a CUDA graph");
   void* scratch = nullptr;
-  tide_status_t st = scratch_for_current_device(&scratch);
+  int dev = 0;
+  tide_status_t st = scratch_for_current_device(&scratch, &dev);
   if (st != TIDE_OK) return st;
 
   const int64_t tiles = (int64_t)l->rs_tiles.size();
@@ -105,12 +130,29 @@ extern "C" TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t l,
     for (int32_t k = 0; k < N; ++k) table[(size_t)p * N + k] = grads[(size_t)k * P + p];
   for (int64_t i = 0; i < (int64_t)N * P; ++i) table[(size_t)N * P + i] = shards[i];
   unsigned char* base = (unsigned char*)scratch;
+  std::lock_guard<std::mutex> hg(g_held_mu);
+  Held& held = g_held[dev];
+  const bool same_tiles = held.serial == l->serial && held.stream == stream;
+  const bool same_table = same_tiles && held.table == table;
   // Pageable sources: each copy returns once the driver holds its own copy of
-  // the bytes, so the host vectors may go out of scope after the calls.
-  cudaError_t e = cudaMemcpyAsync(base, l->rs_tiles.data(), tile_bytes, cudaMemcpyHostToDevice, stream);
-  if (e == cudaSuccess)
+  // the bytes, so the host vectors may go out of scope after the calls.  (The
+  // copy waits for the stream's earlier work, so a call that copies blocks
+  // the host until then; a repeated call copies nothing and returns at once.)
+  cudaError_t e = cudaSuccess;
+  if (!same_tiles) {
+    held.serial = 0;
+    e = cudaMemcpyAsync(base, l->rs_tiles.data(), tile_bytes, cudaMemcpyHostToDevice, stream);
+  }
+  if (e == cudaSuccess && !same_table) {
+    held.serial = 0;
     e = cudaMemcpyAsync(base + tile_bytes, table.data(), table_bytes, cudaMemcpyHostToDevice, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "copy of the tables into the no-allocation scratch");
+  if (!same_table) {
+    held.serial = l->serial;
+    held.stream = stream;
+    held.table.swap(table);
+  }
 
   RsArgs a;
   a.tiles = (const Tile*)base;

@@ -159,6 +159,7 @@ constexpr int kPtrSlots = 8;
 }  // namespace tide
 
 struct tide_layout_s {
+  uint64_t serial = 0;  // unique per layout within the process, never reused
   int32_t num_ranks = 0;
   int32_t num_params = 0;
   int64_t align = 8;

@@ -82,3 +82,60 @@ def test_noalloc_capped_mode_and_size_limit():
                                                  ctypes.addressof(fake), ctypes.c_float(1.0), None)
         assert st == tide.TIDE_ERR_INVALID_ARG
         assert "at most" in tide.tide_last_error()
+
+
+def test_noalloc_repeats_alternating_layouts_pointers_and_streams():
+    """A repeated call on the same stream with the same layout and pointers
+    copies nothing; any change (another layout in between, new output
+    buffers, another stream) copies again.  Every result bit-exact."""
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    wla, wlb = synth.tiny(), synth.custom("small_b", 3, [(37, 24), (5,), (64, 8)], seed=9)
+    with tide.Layout(wla.shapes, wla.num_ranks) as la, tide.Layout(wlb.shapes, wlb.num_ranks) as lb:
+        ja, jb = DeviceJob(wla, la), DeviceJob(wlb, lb)
+        torch.cuda.synchronize()
+        want = {}
+        for lay, job, wl in ((la, ja, wla), (lb, jb, wlb)):
+            lay.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), wl.scale, s1)
+            s1.synchronize()
+            want[id(job)] = _shards(job)
+        calls = [(la, ja, wla, s1), (la, ja, wla, s1), (lb, jb, wlb, s1), (la, ja, wla, s1),
+                 (la, ja, wla, s2), (la, ja, wla, s2), (lb, jb, wlb, s1)]
+        for i, (lay, job, wl, st) in enumerate(calls):
+            job.reset_outputs()
+            torch.cuda.synchronize()
+            assert _call_noalloc(lay, job, wl.scale, st) == tide.TIDE_OK, tide.tide_last_error()
+            st.synchronize()
+            assert all(torch.equal(a, b) for a, b in zip(_shards(job), want[id(job)])), f"call {i}"
+            assert job.guards_intact()
+        # new output buffers, same layout and stream: the pointer table is copied again
+        outs = [[torch.full_like(s, float("nan")) for s in row] for row in ja.shards]
+        g = (ctypes.c_void_p * (ja.N * ja.P))(*[t.data_ptr() for t in ja.grad_ptrs()])
+        o = (ctypes.c_void_p * (ja.N * ja.P))(*[t.data_ptr() for row in outs for t in row])
+        assert T._lib.tide_rs_bf16_to_fp32_noalloc(la.handle, ctypes.addressof(g), ctypes.addressof(o),
+                                                   ctypes.c_float(wla.scale),
+                                                   ctypes.c_void_p(s2.cuda_stream)) == tide.TIDE_OK
+        s2.synchronize()
+        got = [t.view(torch.int32).clone() for row in outs for t in row]
+        assert all(torch.equal(a, b) for a, b in zip(got, want[id(ja)]))
+
+
+def test_noalloc_refused_inside_stream_capture():
+    """Pageable copies cannot be replayed from a graph: inside a capture the
+    call is refused before it enqueues anything, and the capture stays valid."""
+    wl = synth.tiny()
+    with tide.Layout(wl.shapes, wl.num_ranks) as lay:
+        job = DeviceJob(wl, lay)
+        x = torch.zeros(16, device="cuda")
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            graph.capture_begin()
+            x.add_(1.0)
+            st = _call_noalloc(lay, job, wl.scale, s)
+            graph.capture_end()
+        assert st == tide.TIDE_ERR_UNSUPPORTED
+        assert "captured" in tide.tide_last_error()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert float(x[0]) == 1.0

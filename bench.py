@@ -416,9 +416,9 @@ def run_tide(args):
                    "parallelism": f"replicas x{world}"},
         "kernels": {
             "rs": {"ms": round(rs_avg, 4), "GB/s": round(rs_gbs, 1), "frac": round(rs_gbs / peak, 4),
-                   "grid": grid_rs, "block": block_rs},
+                   "ms_median": round(statistics.median(rs_ms), 4), "grid": grid_rs, "block": block_rs},
             "ag": {"ms": round(ag_avg, 4), "GB/s": round(ag_gbs, 1), "frac": round(ag_gbs / peak, 4),
-                   "grid": grid_ag, "block": block_ag},
+                   "ms_median": round(statistics.median(ag_ms), 4), "grid": grid_ag, "block": block_ag},
         },
         "roofline": {"bound": "hbm",
                      "kernel": "tide rs_bulk_kernel" if args.mode == "bulk" else "tide rs_kernel",

@@ -134,9 +134,16 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sel = [ln for ts, ln in self.lines if t0 is None or (t0 - 0.06 <= ts <= t1 + 0.06)]
-        if not sel:
-            sel = [ln for _, ln in self.lines]
+        return self.summary(t0, t1)
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen in [t0, t1] (host time)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        lines = list(self.lines)
+        sel = [ln for ts, ln in lines if t0 is None or (t0 - 0.06 <= ts <= t1 + 0.06)]
+        if not sel and t0 is None:
+            sel = [ln for _, ln in lines]
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in sel:
@@ -369,7 +376,8 @@ def run_tide(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     # nvidia-smi -i takes an index, a UUID or a PCI id: pass the visible entry as is
     visible = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
-    clocks = ClockSampler(visible[dev] if dev < len(visible) else str(dev))
+    smi_dev = visible[dev] if dev < len(visible) else str(dev)
+    clocks = ClockSampler(smi_dev)
     clocks.start()
     time.sleep(0.3)
     barrier(world)
@@ -445,7 +453,7 @@ def run_tide(args):
             out["e2e"] = {"value": None, "unit": "GB/s", "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0, "unavailable": f"{type(e).__name__}: {e}"[:300]}
     if not args.no_interference:
-        out["interference"] = run_interference(tide, layout, job, wl, props)
+        out["interference"] = run_interference(tide, layout, job, wl, props, smi_dev)
     layout.set_mode(tide.TIDE_MODE_UNCAPPED)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, 10.0)
@@ -742,7 +750,7 @@ def run_e2e(tide, layout, job, wl, stream, K, world):
     return out
 
 
-def run_interference(tide, layout, job, wl, props):
+def run_interference(tide, layout, job, wl, props, smi_dev):
     """Slowdown of a bf16 8192^3 GEMM on one stream while the reduce-scatter
     (or placement) loops on another, per mode; the op's bandwidth during the
     GEMM window and its SM.time.  Modes marked `_lowprio` put the GEMM on a
@@ -803,9 +811,14 @@ def run_interference(tide, layout, job, wl, props):
     modes += [("ag", "uncapped", U, 0, False), ("ag", "uncapped_lowprio", U, 0, True),
               ("ag", "bulk_tma", B, 0, False), ("ag", "bulk_tma_lowprio", B, 0, True),
               ("ag", "capped16", C, 16, False), ("ag", "copy_engine", CE, 0, False)]
+    sampler = ClockSampler(smi_dev)
+    sampler.start()
+    time.sleep(0.2)
     for kind, name, mode, cap, prio in modes:
         sg, sr = streams[prio]
-        base = t0_hi if prio else t0
+        w0 = time.time()
+        # the GEMM's own time drifts with its power state: re-measure it beside each mode
+        base = gemm_alone(sg)
         layout.set_mode(mode, cap)
         if kind == "rs":
             def op():
@@ -848,6 +861,7 @@ def run_interference(tide, layout, job, wl, props):
             if en > st:
                 moved += nbytes * max(0.0, min(en, window) - max(st, 0.0)) / (en - st)
         loop_ms = evs[0][0].elapsed_time(evs[-1][1]) / count
+        w1 = time.time()
         grid, _ = layout.launch_shape(opname)
         sm_used = min(grid, props.multi_processor_count) if grid else 0
         res["modes"].append({
@@ -857,10 +871,13 @@ def run_interference(tide, layout, job, wl, props):
             "op_GB/s_alone": round(nbytes / (alone_ms * 1e-3) / 1e9, 1),
             "op_ms_concurrent": round(loop_ms, 4),
             "op_GB/s_during_gemm": round(moved / (window * 1e-3) / 1e9, 1),
+            "gemm_ms_alone": round(base, 4),
             "gemm_ms_concurrent": round(t1, 4),
             "gemm_slowdown_pct": round(100.0 * (t1 / base - 1.0), 2),
             "sm_ms": round(alone_ms * sm_used, 2),
+            "clocks": sampler.summary(w0, w1),
         })
+    res["clocks"] = sampler.stop()
     layout.set_mode(tide.TIDE_MODE_UNCAPPED, 0)
     del a, b, c
     return res

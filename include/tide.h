@@ -61,8 +61,9 @@
  *    one: outside the capped mode every launch is one short-lived CTA per
  *    tile, so the block scheduler dispatches the compute kernel's pending
  *    CTAs first and the collective fills what it leaves (on GB300 a bf16
- *    8192^3 GEMM then runs at its solo speed while the reduce-scatter still
- *    moves ~2.4 TB/s beside it).
+ *    8192^3 GEMM then loses about what 8-16 capped CTAs would cost it,
+ *    -2% to +11%, while the reduce-scatter still moves ~2.4 TB/s beside it,
+ *    2-3.5x what those capped modes move).
  *  - A layout may be used from several host threads (calls are serialised
  *    internally).  Calls on different streams that write the same output
  *    buffers race, as any two kernels would.

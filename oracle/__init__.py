@@ -34,7 +34,7 @@ def lib():
                                     ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, _i64p]
         L.oracle_rs_element.restype = ctypes.c_float
         L.oracle_rs_element.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_float]
-        L.oracle_rs.restype = None
+        L.oracle_rs.restype = ctypes.c_int
         L.oracle_rs.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float]
         L.oracle_ag_place.restype = None
@@ -45,7 +45,7 @@ def lib():
         L.oracle_ag_source_index.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_int64]
-        L.oracle_rs_rank.restype = None
+        L.oracle_rs_rank.restype = ctypes.c_int
         L.oracle_rs_rank.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                      ctypes.c_float, ctypes.c_int32]
@@ -59,7 +59,7 @@ def lib():
         L.oracle_rs_stage.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                       ctypes.c_void_p, ctypes.c_void_p]
-        L.oracle_rs_staged.restype = None
+        L.oracle_rs_staged.restype = ctypes.c_int
         L.oracle_rs_staged.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float]
@@ -80,6 +80,18 @@ def _dims(shapes):
         d0.append(int(s[0]))
         inner.append(n)
     return np.asarray(d0, dtype=np.int64), np.asarray(inner, dtype=np.int64)
+
+
+def _check_ranks(num_ranks: int) -> None:
+    """The C oracle gathers one element's N inputs into a 4096-entry stack
+    array and refuses larger N; refuse here too, with a clear message."""
+    if not 1 <= num_ranks <= MAX_RANKS:
+        raise ValueError(f"oracle supports 1 .. {MAX_RANKS} ranks, got {num_ranks}")
+
+
+def _rc(rc: int, what: str) -> None:
+    if rc != 0:
+        raise ValueError(f"{what} refused its arguments")
 
 
 def _ptrs(arrays):
@@ -118,8 +130,7 @@ def rs_element(vals_bf16: np.ndarray, scale: float) -> float:
 
 def rs(shapes, num_ranks: int, grads, scale: float):
     """grads[k][p]: uint16 arrays (bf16 bits).  Returns shards[r][p] fp32 arrays."""
-    if num_ranks > MAX_RANKS:
-        raise ValueError("oracle supports at most 4096 ranks")
+    _check_ranks(num_ranks)
     P = len(shapes)
     d0, inner = _dims(shapes)
     g = [np.ascontiguousarray(grads[k][p], dtype=np.uint16)
@@ -128,8 +139,8 @@ def rs(shapes, num_ranks: int, grads, scale: float):
                for p in range(P)] for _ in range(num_ranks)]
     flat_out = [shards[r][p] for r in range(num_ranks) for p in range(P)]
     gp, op = _ptrs(g), _ptrs(flat_out)
-    lib().oracle_rs(num_ranks, P, d0.ctypes.data, inner.ctypes.data, gp.ctypes.data,
-                    op.ctypes.data, scale)
+    _rc(lib().oracle_rs(num_ranks, P, d0.ctypes.data, inner.ctypes.data, gp.ctypes.data,
+                        op.ctypes.data, scale), "oracle_rs")
     return shards
 
 
@@ -155,6 +166,9 @@ def ag_source_index(num_ranks, shape, offset, block_numel, i, j) -> int:
 
 def rs_rank(shapes, num_ranks: int, grads, scale: float, r: int):
     """Rank r's shards only: list of P fp32 arrays."""
+    _check_ranks(num_ranks)
+    if not 0 <= r < num_ranks:
+        raise ValueError(f"rank {r} out of range")
     P = len(shapes)
     d0, inner = _dims(shapes)
     g = [np.ascontiguousarray(grads[k][p], dtype=np.uint16)
@@ -162,8 +176,8 @@ def rs_rank(shapes, num_ranks: int, grads, scale: float, r: int):
     out = [np.empty(chunk_rows(int(d0[p]), num_ranks) * int(inner[p]), dtype=np.float32)
            for p in range(P)]
     gp, op = _ptrs(g), _ptrs(out)
-    lib().oracle_rs_rank(num_ranks, P, d0.ctypes.data, inner.ctypes.data, gp.ctypes.data,
-                         op.ctypes.data, scale, r)
+    _rc(lib().oracle_rs_rank(num_ranks, P, d0.ctypes.data, inner.ctypes.data, gp.ctypes.data,
+                             op.ctypes.data, scale, r), "oracle_rs_rank")
     return out
 
 
@@ -205,6 +219,7 @@ def rs_stage(shapes, num_ranks: int, offsets, block_numel: int, grads_k, slot):
 
 def rs_staged(shapes, num_ranks: int, offsets, block_numel: int, slots, scale: float):
     """Reduce-scatter from N staged slots; returns shards[r][p]."""
+    _check_ranks(num_ranks)
     P = len(shapes)
     d0, inner = _dims(shapes)
     sl = [np.ascontiguousarray(x, dtype=np.uint16) for x in slots]
@@ -213,6 +228,6 @@ def rs_staged(shapes, num_ranks: int, offsets, block_numel: int, slots, scale: f
                for p in range(P)] for _ in range(num_ranks)]
     flat = [shards[r][p] for r in range(num_ranks) for p in range(P)]
     sp, op = _ptrs(sl), _ptrs(flat)
-    lib().oracle_rs_staged(num_ranks, P, d0.ctypes.data, inner.ctypes.data, offs.ctypes.data,
-                           block_numel, sp.ctypes.data, op.ctypes.data, scale)
+    _rc(lib().oracle_rs_staged(num_ranks, P, d0.ctypes.data, inner.ctypes.data, offs.ctypes.data,
+                               block_numel, sp.ctypes.data, op.ctypes.data, scale), "oracle_rs_staged")
     return shards

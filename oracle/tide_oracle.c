@@ -18,6 +18,10 @@ static float bf16_to_f32(uint16_t b) {
 
 static int64_t roundup(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
+/* Each reduced element gathers its N inputs into a stack array of this many
+ * entries; the reduce-scatter functions refuse larger N before touching it. */
+#define ORACLE_MAX_RANKS 4096
+
 /* FSDP2 dim-0 chunking (reading: torch.chunk sizes padded to N chunks). */
 int64_t oracle_chunk_rows(int64_t d0, int32_t num_ranks) {
   return (d0 + num_ranks - 1) / num_ranks;
@@ -57,9 +61,10 @@ float oracle_rs_element(int32_t num_ranks, const uint16_t* vals, float scale) {
 /* Reduce-scatter ([TIDE] "FSDP2通信开销的根源"; [VOL] "分片中的通信原语"):
  * every rank holds a full gradient of each parameter; afterwards rank r holds
  * the reduced values of its own dim-0 chunk only. */
-void oracle_rs(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
-               const uint16_t* const* grads, float* const* shards, float scale) {
-  uint16_t vals[4096];
+int oracle_rs(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+              const uint16_t* const* grads, float* const* shards, float scale) {
+  uint16_t vals[ORACLE_MAX_RANKS];
+  if (num_ranks < 1 || num_ranks > ORACLE_MAX_RANKS) return 1;
   for (int32_t p = 0; p < num_params; ++p) {
     const int64_t c = oracle_chunk_rows(d0[p], num_ranks);
     for (int32_t r = 0; r < num_ranks; ++r) {
@@ -78,6 +83,7 @@ void oracle_rs(int32_t num_ranks, int32_t num_params, const int64_t* d0, const i
       }
     }
   }
+  return 0;
 }
 
 int64_t oracle_ag_source_index(int32_t num_ranks, int64_t d0, int64_t inner, int64_t offset,
@@ -101,9 +107,10 @@ void oracle_ag_place(int32_t num_ranks, int32_t num_params, const int64_t* d0,
                                             i, j)];
 }
 
-void oracle_rs_rank(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
-                    const uint16_t* const* grads, float* const* shards_r, float scale, int32_t r) {
-  uint16_t vals[4096];
+int oracle_rs_rank(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                   const uint16_t* const* grads, float* const* shards_r, float scale, int32_t r) {
+  uint16_t vals[ORACLE_MAX_RANKS];
+  if (num_ranks < 1 || num_ranks > ORACLE_MAX_RANKS || r < 0 || r >= num_ranks) return 1;
   for (int32_t p = 0; p < num_params; ++p) {
     const int64_t c = oracle_chunk_rows(d0[p], num_ranks);
     for (int64_t ii = 0; ii < c; ++ii) {
@@ -119,6 +126,7 @@ void oracle_rs_rank(int32_t num_ranks, int32_t num_params, const int64_t* d0, co
       }
     }
   }
+  return 0;
 }
 
 /* Round to nearest even on the 16 bits dropped: add half an ulp of bf16
@@ -156,10 +164,11 @@ void oracle_rs_stage(int32_t num_ranks, int32_t num_params, const int64_t* d0, c
   }
 }
 
-void oracle_rs_staged(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
-                      const int64_t* offsets, int64_t block_numel, const uint16_t* const* slots,
-                      float* const* shards, float scale) {
-  uint16_t vals[4096];
+int oracle_rs_staged(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                     const int64_t* offsets, int64_t block_numel, const uint16_t* const* slots,
+                     float* const* shards, float scale) {
+  uint16_t vals[ORACLE_MAX_RANKS];
+  if (num_ranks < 1 || num_ranks > ORACLE_MAX_RANKS) return 1;
   for (int32_t p = 0; p < num_params; ++p) {
     const int64_t c = oracle_chunk_rows(d0[p], num_ranks);
     for (int32_t r = 0; r < num_ranks; ++r) {
@@ -176,4 +185,5 @@ void oracle_rs_staged(int32_t num_ranks, int32_t num_params, const int64_t* d0, 
       }
     }
   }
+  return 0;
 }

@@ -63,9 +63,11 @@ float oracle_rs_element(int32_t num_ranks, const uint16_t* vals, float scale);
 /* Reduce-scatter of bf16 per-parameter gradients into fp32 dim-0 shards.
  * grads[k * P + p]: rank k's gradient of parameter p, d0[p] * inner[p] bf16.
  * shards[r * P + p]: rank r's shard of parameter p, c_p * inner[p] fp32;
- * rows past d0[p] are written +0.0f. */
-void oracle_rs(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
-               const uint16_t* const* grads, float* const* shards, float scale);
+ * rows past d0[p] are written +0.0f.  Returns 0, or 1 without writing
+ * anything when num_ranks is outside 1 .. 4096 (the size of the per-element
+ * stack array of inputs). */
+int oracle_rs(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+              const uint16_t* const* grads, float* const* shards, float scale);
 
 /* Placement of a rank-major gathered bf16 buffer (num_ranks * block_numel
  * elements) into per-parameter storage params[p] (d0[p] * inner[p] bf16). */
@@ -79,9 +81,11 @@ int64_t oracle_ag_source_index(int32_t num_ranks, int64_t d0, int64_t inner, int
                                int64_t block_numel, int64_t i, int64_t j);
 
 /* Reduce-scatter output of one rank only: shards_r[p] (c_p * inner[p] fp32)
- * receives exactly what oracle_rs writes to shards[r * P + p]. */
-void oracle_rs_rank(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
-                    const uint16_t* const* grads, float* const* shards_r, float scale, int32_t r);
+ * receives exactly what oracle_rs writes to shards[r * P + p].  Returns 0,
+ * or 1 without writing anything when num_ranks is outside 1 .. 4096 or r is
+ * not a rank. */
+int oracle_rs_rank(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                   const uint16_t* const* grads, float* const* shards_r, float scale, int32_t r);
 
 /* fp32 -> bf16 bits, round to nearest, ties to even; NaN keeps its sign and
  * top payload bits and becomes quiet; overflow rounds to infinity. */
@@ -107,10 +111,12 @@ void oracle_rs_stage(int32_t num_ranks, int32_t num_params, const int64_t* d0, c
 
 /* Reduce-scatter from the N staged slots:
  *   shards[r * P + p][e] = scale * sum_{k=0}^{N-1} f32(slots[k][r * S + o_p + e])  for e < v_{p,r} * inner[p],
- *   +0.0f for the padding rows; fp32 sum in ascending k from +0.0f. */
-void oracle_rs_staged(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
-                      const int64_t* offsets, int64_t block_numel, const uint16_t* const* slots,
-                      float* const* shards, float scale);
+ *   +0.0f for the padding rows; fp32 sum in ascending k from +0.0f.
+ * Returns 0, or 1 without writing anything when num_ranks is outside
+ * 1 .. 4096. */
+int oracle_rs_staged(int32_t num_ranks, int32_t num_params, const int64_t* d0, const int64_t* inner,
+                     const int64_t* offsets, int64_t block_numel, const uint16_t* const* slots,
+                     float* const* shards, float scale);
 
 #ifdef __cplusplus
 }

@@ -90,7 +90,7 @@ int main(void) {
   uint16_t* op[P];
   for (int i = 0; i < N * P; ++i) os[i] = malloc(sizeof(float) * shard_n[i % P]);
   for (int p = 0; p < P; ++p) op[p] = malloc(sizeof(uint16_t) * numel[p]);
-  oracle_rs(N, P, d0, inner, (const uint16_t* const*)hg, os, 0.25f);
+  if (oracle_rs(N, P, d0, inner, (const uint16_t* const*)hg, os, 0.25f) != 0) return fail("oracle_rs refused");
   oracle_ag_place(N, P, d0, inner, offs, S, hbuf, op);
 
   long bad = 0, checked = 0;

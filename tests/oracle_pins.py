@@ -445,3 +445,49 @@ def check_staged_rs_equals_rs(seed=12):
 
 
 ALL_CHECKS += [check_stage_is_inverse_of_placement, check_staged_rs_equals_rs]
+
+
+def check_rs_rank_limit():
+    """The reduce-scatter functions gather one element's N inputs into a
+    4096-entry array: N = 4096 is computed (and equals the exact integer
+    sum), N = 4097 and N = 0 are refused before anything is read or written,
+    through the wrapper and through the C entry points themselves."""
+    import ctypes
+
+    one = 0x3F80  # bf16 1.0
+    n = 4096
+    grads = [[np.array([one], dtype=np.uint16)] for _ in range(n)]
+    out = oracle.rs([(1,)], n, grads, 1.0)
+    assert out[0][0][0] == np.float32(n) and all(out[r][0].size == 1 and out[r][0][0] == 0 for r in range(1, n))
+    assert oracle.rs_rank([(1,)], n, grads, 1.0, 0)[0][0] == np.float32(n)
+    for bad in (n + 1, 0):
+        for call in (lambda: oracle.rs([(1,)], bad, grads, 1.0),
+                     lambda: oracle.rs_rank([(1,)], bad, grads, 1.0, 0),
+                     lambda: oracle.rs_staged([(1,)], bad, [0], 8, [], 1.0)):
+            try:
+                call()
+            except ValueError:
+                continue
+            raise AssertionError(f"oracle accepted {bad} ranks")
+    # the C functions refuse on their own (the wrapper is not the only guard)
+    L = oracle.lib()
+    n = 4097
+    d0 = np.ones(1, dtype=np.int64)
+    inner = np.ones(1, dtype=np.int64)
+    src = np.array([one], dtype=np.uint16)
+    gp = np.full(n, src.ctypes.data, dtype=np.uint64)
+    outs = [np.full(1, 7.0, dtype=np.float32) for _ in range(n)]
+    op = np.asarray([o.ctypes.data for o in outs], dtype=np.uint64)
+    offs = np.zeros(1, dtype=np.int64)
+    assert L.oracle_rs(n, 1, d0.ctypes.data, inner.ctypes.data, gp.ctypes.data, op.ctypes.data,
+                       ctypes.c_float(1.0)) == 1
+    assert L.oracle_rs_rank(n, 1, d0.ctypes.data, inner.ctypes.data, gp.ctypes.data, op.ctypes.data,
+                            ctypes.c_float(1.0), 0) == 1
+    assert L.oracle_rs_staged(n, 1, d0.ctypes.data, inner.ctypes.data, offs.ctypes.data, 8,
+                              gp.ctypes.data, op.ctypes.data, ctypes.c_float(1.0)) == 1
+    assert L.oracle_rs_rank(4, 1, d0.ctypes.data, inner.ctypes.data, gp.ctypes.data, op.ctypes.data,
+                            ctypes.c_float(1.0), 4) == 1
+    assert all(o[0] == 7.0 for o in outs), "a refused call wrote an output"
+
+
+ALL_CHECKS += [check_rs_rank_limit]

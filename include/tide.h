@@ -44,16 +44,24 @@
  *    the call.  The caller owns every device buffer
  *    and keeps it alive until the work enqueued on `stream` completes.
  *  - Compute calls are asynchronous with respect to the host and never
- *    synchronise the device.  The first compute call of a layout uploads its
- *    tables to the device (allocating them), and the first call with a new
- *    set of pointers uploads that pointer table; after one such call on a
- *    stream, the same calls with the same pointers can be captured from that
- *    stream into a CUDA graph and replayed (tested for tide_rs_bf16_to_fp32
- *    and tide_ag_place).  A pointer set used for the first time inside a
- *    capture is refused (TIDE_ERR_UNSUPPORTED); the device table of a pointer
- *    set used inside a capture is kept unchanged for the layout's lifetime
- *    (at most 8 pointer sets per layout can be held that way), so destroy
- *    the layout only once such graphs are no longer replayed.
+ *    synchronise the device; every copy they make is cudaMemcpyAsync from
+ *    pinned staging on the caller's stream.  The first compute call of a
+ *    layout allocates its device tables and uploads its tile lists on its
+ *    stream (calls on other streams are ordered after that upload); the
+ *    first call with a new set of pointers uploads that pointer table into
+ *    one of 8 cached slots per layout, each allocated once at its largest
+ *    size, so no call frees device memory before tide_layout_destroy.  The
+ *    host waits in one case only: a new pointer set that finds all 8 slots
+ *    holding other sets waits for the last kernel that read the least
+ *    recently used one before overwriting it.  After one call on a stream,
+ *    the same calls with the same pointers can be captured from that stream
+ *    into a CUDA graph and replayed (tested for tide_rs_bf16_to_fp32 and
+ *    tide_ag_place).  A layout's first compute call, and a pointer set used
+ *    for the first time, are refused inside a capture
+ *    (TIDE_ERR_UNSUPPORTED); the device table of a pointer set used inside a
+ *    capture is kept unchanged for the layout's lifetime (at most 8 pointer
+ *    sets per layout can be held that way), so destroy the layout only once
+ *    such graphs are no longer replayed.
  *  - A failed CUDA call is reported through the status and cleared from the
  *    runtime's per-thread last error.
  *  - Next to compute kernels, enqueue the calls on a low-priority stream
@@ -339,17 +347,22 @@ TIDE_API tide_status_t tide_rs_staged_bf16_to_fp32(tide_layout_t layout, const u
  * array of TIDE_NOALLOC_SCRATCH_BYTES (4 MiB) that every GPU loading the
  * library holds until the process exits; a layout that needs more returns
  * TIDE_ERR_INVALID_ARG without enqueuing anything.  Every byte the kernel
- * reads from the array is written by the same call, so nothing has to start
- * at zero.  All calls share the array, which keeps the last call's tables:
- * calls that overlap on the GPU (on different streams, or from different
- * layouts without stream ordering between them) race.  The first call on
- * each device looks up the array's device address (cudaGetSymbolAddress).
- * The tables are copied from pageable host memory, so a call that copies
- * returns only once the stream's earlier work has completed and the driver
- * has taken its copy of them.  A call on the same stream, with the same
- * layout and the same pointers as the call that last filled the array,
- * copies nothing and returns at once (stream order already puts the
- * earlier copies before its kernel).  Inside a stream capture the call
+ * reads from the array was written either by this call or by the last call
+ * that copied into it, whose copies stream order puts ahead of this kernel,
+ * so nothing has to start at zero.  All calls share the array, which keeps
+ * the last call's tables: calls that overlap on the GPU (on different
+ * streams, or from different layouts without stream ordering between them)
+ * race.  The first call on each device, and the first after the device's
+ * CUDA context was replaced (cudaDeviceReset), looks up the array's device
+ * address (cudaGetSymbolAddress) and copies the tables again.  The tables
+ * are copied from pageable host memory, so a call that copies returns only
+ * once the stream's earlier work has completed and the driver has taken
+ * its copy of them; calls on one device are serialised with each other
+ * (one lock per device) while they check, copy and launch, and calls on
+ * different devices do not wait for each other.  A call on the same stream,
+ * with the same layout and the same pointers as the call that last filled
+ * the array, copies nothing and returns at once (stream order already puts
+ * the earlier copies before its kernel).  Inside a stream capture the call
  * returns TIDE_ERR_UNSUPPORTED: pageable copies cannot be replayed from a
  * CUDA graph.  No cudaMalloc, cudaFree or other allocating routine is
  * called.

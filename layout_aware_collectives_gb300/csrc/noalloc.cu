@@ -13,6 +13,7 @@
 // The kernel's scratch (tile list + gradient and shard pointer tables) lives
 // in one file-scope __device__ array of kNoallocScratchBytes that every GPU
 // loading this library holds until the process exits.
+#include <cuda.h>  // driver-API types only; the entry points are fetched through the runtime
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -30,40 +31,82 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device.  In host
-// code the symbol name is only a host-side stand-in, never a device address.
-std::mutex g_setup_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// What each device's array holds: the tile list of layout `serial` and a
+// What one device's array holds: the tile list of layout `serial` and a
 // pointer table, both copied on `stream`.  A later call on the same stream
 // with the same layout and pointers skips the copies, since stream order
 // already puts them before its kernel (a stream handle is only handed out
-// again after the destroyed stream's work has completed).  Guarded by
-// g_held_mu, held from the check through the kernel launch.
+// again after the destroyed stream's work has completed).
 struct Held {
   uint64_t serial = 0;  // 0: nothing known to be there
   cudaStream_t stream = nullptr;
   std::vector<const void*> table;
 };
-std::mutex g_held_mu;
-Held g_held[kMaxDevices];
 
-tide_status_t scratch_for_current_device(void** out, int* dev_out) {
+// Per device: the array's device address in the current CUDA context (in
+// host code the symbol name is only a host-side stand-in, never a device
+// address) and what the array holds.  Both belong to one context: after a
+// cudaDeviceReset the module is loaded again, so the address may differ and
+// the contents are gone; a new context id clears them.  `mu` is held from
+// the check through the kernel launch, so copying calls serialise per device
+// and never across devices.
+struct DeviceState {
+  std::mutex mu;
+  void* addr = nullptr;
+  unsigned long long ctx = 0;  // id of the context `addr` and `held` belong to
+  Held held;
+};
+DeviceState g_dev[kMaxDevices];
+
+// Id of the calling thread's current context (unique for the process's
+// lifetime), 0 if none is current or the driver cannot tell.
+using CtxGetCurrent = CUresult (*)(CUcontext*);
+using CtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+std::once_flag g_entry_once;
+CtxGetCurrent g_ctx_get_current = nullptr;
+CtxGetId g_ctx_get_id = nullptr;
+
+unsigned long long current_context_id() {
+  std::call_once(g_entry_once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = (CtxGetCurrent)f;
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = (CtxGetId)f;
+    cudaGetLastError();
+  });
+  if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  if (g_ctx_get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// The current device's state, with its `mu` locked by `lock` and its address
+// valid for the current context.
+tide_status_t device_state(std::unique_lock<std::mutex>* lock, DeviceState** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices)
     return set_error(TIDE_ERR_UNSUPPORTED, "device ordinal beyond the no-allocation table");
-  std::lock_guard<std::mutex> g(g_setup_mu);
-  if (!g_scratch_addr[dev]) {
+  DeviceState& d = g_dev[dev];
+  *lock = std::unique_lock<std::mutex>(d.mu);
+  unsigned long long ctx = current_context_id();
+  if (!d.addr || ctx == 0 || ctx != d.ctx) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // also makes the runtime's context current
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
-    g_scratch_addr[dev] = p;
+    ctx = current_context_id();
+    if (ctx == 0 || ctx != d.ctx) d.held = Held();  // another context: the contents are not ours
+    d.addr = p;
+    d.ctx = ctx;
   }
-  *out = g_scratch_addr[dev];
-  *dev_out = dev;
+  *out = &d;
   return TIDE_OK;
 }
 
@@ -114,9 +157,9 @@ extern "C" TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t l,
     return set_error(TIDE_ERR_UNSUPPORTED,
                      "the no-allocation entry point copies its tables from pageable host memory "
                      "and cannot be captured into a CUDA graph");
-  void* scratch = nullptr;
-  int dev = 0;
-  tide_status_t st = scratch_for_current_device(&scratch, &dev);
+  std::unique_lock<std::mutex> dev_lock;
+  DeviceState* ds = nullptr;
+  tide_status_t st = device_state(&dev_lock, &ds);
   if (st != TIDE_OK) return st;
 
   const int64_t tiles = (int64_t)l->rs_tiles.size();
@@ -129,9 +172,8 @@ extern "C" TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t l,
   for (int32_t p = 0; p < P; ++p)
     for (int32_t k = 0; k < N; ++k) table[(size_t)p * N + k] = grads[(size_t)k * P + p];
   for (int64_t i = 0; i < (int64_t)N * P; ++i) table[(size_t)N * P + i] = shards[i];
-  unsigned char* base = (unsigned char*)scratch;
-  std::lock_guard<std::mutex> hg(g_held_mu);
-  Held& held = g_held[dev];
+  unsigned char* base = (unsigned char*)ds->addr;
+  Held& held = ds->held;
   const bool same_tiles = held.serial == l->serial && held.stream == stream;
   const bool same_table = same_tiles && held.table == table;
   // Pageable sources: each copy returns once the driver holds its own copy of

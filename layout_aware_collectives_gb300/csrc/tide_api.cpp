@@ -79,29 +79,53 @@ void release_device(tide_layout_s* l) {
   }
   if (l->d_err) cudaFree(l->d_err);
   l->d_err = nullptr;
+  if (l->tables_ev) {
+    cudaEventSynchronize(l->tables_ev);  // the upload reads the staging
+    cudaEventDestroy(l->tables_ev);
+  }
+  l->tables_ev = nullptr;
+  if (l->h_tile_staging) cudaFreeHost(l->h_tile_staging);
+  l->h_tile_staging = nullptr;
+  l->tables_stream = nullptr;
+  l->tables_resident = false;
   cudaGetLastError();  // leave no error of the clean-up behind
 }
 
-tide_status_t bind_device(tide_layout_s* l, int dev);
+tide_status_t bind_device(tide_layout_s* l, int dev, cudaStream_t stream);
 
-// Bind the layout to the current device on first use: query the SM count,
-// upload the tile lists.  On failure everything allocated so
-// far is released and the layout stays unbound.
-tide_status_t ensure_device(tide_layout_s* l) {
+// Bind the layout to the current device on first use (query the SM count,
+// upload the tile lists on `stream`); later, order a call on another stream
+// after that upload until it has been seen complete.  On failure everything
+// allocated so far is released and the layout stays unbound.
+tide_status_t ensure_device(tide_layout_s* l, cudaStream_t stream) {
   int dev = 0;
   TIDE_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
   if (l->device >= 0) {
     if (dev != l->device)
       return set_error(TIDE_ERR_INVALID_ARG, "layout is bound to device " + std::to_string(l->device) +
                                                  " but device " + std::to_string(dev) + " is current");
+    if (!l->tables_resident && stream != l->tables_stream && !capturing(stream)) {
+      const cudaError_t q = cudaEventQuery(l->tables_ev);
+      if (q == cudaSuccess) {
+        l->tables_resident = true;
+      } else if (q == cudaErrorNotReady) {
+        TIDE_CUDA(cudaStreamWaitEvent(stream, l->tables_ev, 0), "cudaStreamWaitEvent");
+      } else {
+        return cuda_fail(q, "cudaEventQuery(tile-list upload)");
+      }
+    }
     return TIDE_OK;
   }
-  tide_status_t st = bind_device(l, dev);
+  if (capturing(stream))
+    return set_error(TIDE_ERR_UNSUPPORTED,
+                     "the layout's first compute call sets it up on the device and cannot be captured; "
+                     "make one call on this stream before capturing");
+  tide_status_t st = bind_device(l, dev, stream);
   if (st != TIDE_OK) release_device(l);
   return st;
 }
 
-tide_status_t bind_device(tide_layout_s* l, int dev) {
+tide_status_t bind_device(tide_layout_s* l, int dev, cudaStream_t stream) {
   DeviceShape d;
   tide_status_t st = query_device(&d);
   if (st != TIDE_OK) return st;
@@ -115,16 +139,28 @@ tide_status_t bind_device(tide_layout_s* l, int dev) {
                 {&l->ag_tiles, &l->d_ag_tiles, "placement tile list"},
                 {&l->pk_tiles, &l->d_pk_tiles, "pack tile list"},
                 {&l->st_tiles, &l->d_st_tiles, "staged reduce-scatter tile list"}};
+  // One pinned staging buffer for the four lists: the copies are then
+  // asynchronous (a pageable source would make the host wait for the stream).
+  size_t total = 0;
+  for (auto& t : lists) total += t.host->size();
+  TIDE_CUDA(cudaMallocHost(&l->h_tile_staging, sizeof(Tile) * std::max<size_t>(1, total)),
+            "cudaMallocHost(tile-list staging)");
+  Tile* staged = (Tile*)l->h_tile_staging;
   for (auto& t : lists) {
     TIDE_CUDA(cudaMalloc((void**)t.dev, sizeof(Tile) * std::max<size_t>(1, t.host->size())),
               "cudaMalloc(tile list)");
-    if (!t.host->empty())
-      TIDE_CUDA(cudaMemcpy(*t.dev, t.host->data(), sizeof(Tile) * t.host->size(),
-                           cudaMemcpyHostToDevice),
+    if (!t.host->empty()) {
+      std::memcpy(staged, t.host->data(), sizeof(Tile) * t.host->size());
+      TIDE_CUDA(cudaMemcpyAsync(*t.dev, staged, sizeof(Tile) * t.host->size(), cudaMemcpyHostToDevice, stream),
                 t.what);
+      staged += t.host->size();
+    }
   }
   TIDE_CUDA(cudaMalloc((void**)&l->d_err, sizeof(int)), "cudaMalloc(error word)");
-  TIDE_CUDA(cudaMemset(l->d_err, 0, sizeof(int)), "cudaMemset(error word)");
+  TIDE_CUDA(cudaMemsetAsync(l->d_err, 0, sizeof(int), stream), "cudaMemsetAsync(error word)");
+  TIDE_CUDA(cudaEventCreateWithFlags(&l->tables_ev, cudaEventDisableTiming), "cudaEventCreate");
+  TIDE_CUDA(cudaEventRecord(l->tables_ev, stream), "cudaEventRecord");
+  l->tables_stream = stream;
   for (PtrSlot& s : l->slots) {
     TIDE_CUDA(cudaEventCreateWithFlags(&s.upload_ev, cudaEventDisableTiming), "cudaEventCreate");
     TIDE_CUDA(cudaEventCreateWithFlags(&s.use_ev, cudaEventDisableTiming), "cudaEventCreate");
@@ -219,13 +255,12 @@ tide_status_t acquire_table(tide_layout_s* l, const TableKey& key, size_t n_entr
   s->used = false;
   s->use_stream = nullptr;
   s->use_recorded = false;
-  const size_t n = std::max<size_t>(1, n_entries);
-  if (s->capacity < n) {
-    if (s->d_table) cudaFree(s->d_table);
-    if (s->h_staging) cudaFreeHost(s->h_staging);
-    s->d_table = nullptr;
-    s->h_staging = nullptr;
-    s->capacity = 0;
+  // A slot is allocated on its first use at the largest table any operation
+  // needs (2*N*P entries), so no later call frees device memory (a cudaFree
+  // would synchronise the device).
+  const size_t n = std::max<size_t>(1, 2 * (size_t)l->num_ranks * (size_t)l->num_params);
+  if (n_entries > n) return set_error(TIDE_ERR_INVALID_ARG, "pointer table larger than 2*N*P entries");
+  if (s->capacity == 0) {
     TIDE_CUDA(cudaMalloc((void**)&s->d_table, n * sizeof(void*)), "cudaMalloc(pointer table)");
     TIDE_CUDA(cudaMallocHost((void**)&s->h_staging, n * sizeof(void*)),
               "cudaMallocHost(pointer table staging)");
@@ -339,7 +374,7 @@ template <typename Build>
 tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, const TableKey& key, Build&& build,
                      float scale, cudaStream_t stream) {
   if (t1 <= t0) return TIDE_OK;
-  tide_status_t st = ensure_device(l);
+  tide_status_t st = ensure_device(l, stream);
   if (st != TIDE_OK) return st;
   const int64_t NP = (int64_t)l->num_ranks * l->num_params;
   PtrSlot* slot = nullptr;
@@ -508,7 +543,7 @@ tide_status_t tide_ag_place(tide_layout_t l, const uint16_t* gathered, uint16_t*
     if (st != TIDE_OK) return st;
   }
   if (l->ag_tiles.empty()) return TIDE_OK;
-  st = ensure_device(l);
+  st = ensure_device(l, stream);
   if (st != TIDE_OK) return st;
   if (l->mode == TIDE_MODE_COPY_ENGINE)
     return copy_engine(l, const_cast<uint16_t*>(gathered), params, false, stream);
@@ -549,7 +584,7 @@ tide_status_t tide_ag_pack_bf16(tide_layout_t l, int32_t rank, const float* cons
   const int64_t t0 = rank < 0 ? 0 : l->pk_rank_begin[rank];
   const int64_t t1 = rank < 0 ? (int64_t)l->pk_tiles.size() : l->pk_rank_begin[rank + 1];
   if (t1 <= t0) return TIDE_OK;
-  st = ensure_device(l);
+  st = ensure_device(l, stream);
   if (st != TIDE_OK) return st;
 
   const TableKey key = make_key(TIDE_OP_PACK, rank, (const void* const*)shards, (size_t)nin, nullptr, 0);
@@ -591,7 +626,7 @@ tide_status_t tide_rs_stage_bf16(tide_layout_t l, const uint16_t* const* grads, 
     if (st != TIDE_OK) return st;
   }
   if (l->ag_tiles.empty()) return TIDE_OK;
-  st = ensure_device(l);
+  st = ensure_device(l, stream);
   if (st != TIDE_OK) return st;
   if (l->mode == TIDE_MODE_COPY_ENGINE)
     return copy_engine(l, slot, const_cast<uint16_t* const*>(grads), true, stream);

@@ -180,6 +180,13 @@ struct tide_layout_s {
   tide::Tile* d_st_tiles = nullptr;  // RS tiles whose sources are slot offsets
   int num_sms = 0;
   int* d_err = nullptr;         // device error word of the bulk-copy kernels
+  // The tile lists and error word are uploaded on the stream of the first
+  // compute call, from pinned staging kept until destroy; calls on other
+  // streams wait on tables_ev until it has been seen complete.
+  void* h_tile_staging = nullptr;
+  cudaEvent_t tables_ev = nullptr;
+  cudaStream_t tables_stream = nullptr;
+  bool tables_resident = false;
   int64_t test_stall_ns = 0;    // test hook of the bounded waits
   int max_pitch = 0;
   tide::PtrSlot slots[tide::kPtrSlots];

@@ -58,6 +58,9 @@ class Layout:
     def reduce_scatter(self, grads, shards, scale: float, stream=None) -> None:
         _t.tide_rs_bf16_to_fp32(self.handle, grads, shards, scale, stream)
 
+    def reduce_scatter_noalloc(self, grads, shards, scale: float, stream=None) -> None:
+        _t.tide_rs_bf16_to_fp32_noalloc(self.handle, grads, shards, scale, stream)
+
     def reduce_scatter_rank(self, rank: int, grads, shards, scale: float, stream=None) -> None:
         _t.tide_rs_bf16_to_fp32_rank(self.handle, rank, grads, shards, scale, stream)
 

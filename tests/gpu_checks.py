@@ -91,27 +91,32 @@ def sample_indices(rng, job, p, r, per=6):
     return np.array(sorted(pts), dtype=np.int64)
 
 
-def sampled_check_rs(job, seed=0, per=6, scale=None):
+def sampled_check_rs(job, seed=0, per=6, scale=None, ranks=None, outputs=None):
     """Sampled shard elements of every (rank, param) against the oracle, one
-    element at a time from host-regenerated inputs."""
+    element at a time from host-regenerated inputs.  `ranks` restricts the
+    check to some ranks; `outputs[r]` (P tensors) replaces job.shards[r],
+    e.g. the output of a single-rank reduce-scatter."""
     wl = job.wl
     scale = wl.scale if scale is None else scale
+    ranks = list(range(job.N)) if ranks is None else list(ranks)
+    outputs = {} if outputs is None else outputs
     rng = np.random.default_rng(seed)
     checked = 0
     for p in range(job.P):
         d0, inner = job.dims[p]
         c = job.chunk[p]
-        per_rank = [sample_indices(rng, job, p, r, per) for r in range(job.N)]
-        rows = [r * c * inner + idx for r, idx in enumerate(per_rank)]
+        per_rank = [sample_indices(rng, job, p, r, per) for r in ranks]
+        rows = [r * c * inner + idx for r, idx in zip(ranks, per_rank)]
         # source index of every sample in the full gradient
         src = np.concatenate(rows) if rows else np.zeros(0, np.int64)
         valid = src < d0 * inner
         vals = np.stack([wl.host_grad_at(k, p, np.where(valid, src, 0)) for k in range(job.N)])
         pos = 0
-        for r, idx in enumerate(per_rank):
+        for r, idx in zip(ranks, per_rank):
             if idx.size == 0:
                 continue
-            got = _bits32(job.shards[r][p][torch.from_numpy(idx).to(job.device)])
+            shard = outputs[r][p] if r in outputs else job.shards[r][p]
+            got = _bits32(shard[torch.from_numpy(idx).to(job.device)])
             for t, e in enumerate(idx):
                 if valid[pos + t]:
                     want = np.float32(oracle.rs_element(vals[:, pos + t], scale))

@@ -491,3 +491,30 @@ def check_rs_rank_limit():
 
 
 ALL_CHECKS += [check_rs_rank_limit]
+
+
+def check_rs_ieee_closed_forms():
+    """Every special-value case of ieee_cases against its closed form, derived
+    by hand from the sequential fp32 sum: subnormal sums kept (no flush),
+    -0 inputs giving +0, infinities and NaNs propagated, overflow to
+    infinity, and the cases whose result depends on ascending rank order."""
+    import math
+
+    import ieee_cases
+
+    for n in (1, 2, 3, 4, 5, 8, 13, 64, 100):
+        names = [c[0] for c in ieee_cases.cases(n)]
+        cols = np.array([v for _, v in ieee_cases.cases(n)], dtype=np.uint16).T  # [N][C]
+        grads = [[np.ascontiguousarray(cols[k])] for k in range(n)]
+        for scale in (1.0, 0.25, 2.0 ** -6):
+            got = oracle.rs([(1, len(names))], n, grads, scale)[0][0]
+            for j, name in enumerate(names):
+                want = ieee_cases.expected(name, n, scale)
+                g = float(got[j])
+                if math.isnan(want):
+                    assert math.isnan(g), (name, n, scale, g)
+                else:
+                    assert g == want and math.copysign(1, g) == math.copysign(1, want), (name, n, scale, g, want)
+
+
+ALL_CHECKS += [check_rs_ieee_closed_forms]

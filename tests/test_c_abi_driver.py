@@ -12,6 +12,7 @@ INC = os.path.join(ROOT, "include")
 CUDA_INC = "/usr/local/cuda/include"
 CUDA_LIB = "/usr/local/cuda/lib64"
 SRC = os.path.join(ROOT, "tests", "c_driver", "tide_c_driver.c")
+RESET_SRC = os.path.join(ROOT, "tests", "c_driver", "noalloc_reset.c")
 
 
 @pytest.mark.parametrize("lang", ["c", "c++"])
@@ -33,10 +34,20 @@ def build_driver(out):
     subprocess.run(cmd, check=True)
 
 
+def build_reset_driver(out):
+    """The no-allocation entry point across a device reset (needs only
+    libtide and the CUDA runtime)."""
+    d = os.path.join(ROOT, "layout_aware_collectives_gb300")
+    subprocess.run(["gcc", "-std=c11", "-O2", "-Wall", "-I", INC, "-I", CUDA_INC, RESET_SRC, "-o", str(out),
+                    "-L", d, "-Wl,-rpath," + d, "-L", CUDA_LIB, "-Wl,-rpath," + CUDA_LIB, "-ltide", "-lcudart"],
+                   check=True)
+
+
 def test_driver_builds(tmp_path):
     if not shutil.which("gcc"):
         pytest.skip("no C compiler")
     build_driver(tmp_path / "driver")
+    build_reset_driver(tmp_path / "reset_driver")
 
 
 @pytest.mark.gpu

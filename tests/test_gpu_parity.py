@@ -159,6 +159,14 @@ def test_ragged_shapes_full_parity(case, align):
             gpu_checks.full_check_rs(job, scale=0.3)
             gpu_checks.full_check_ag(job)
             assert job.guards_intact()
+        # copy-engine placement: 2-D copies for the ranks with a full chunk, one
+        # copy for a partial chunk, nothing for empty ranks or zero-size tensors
+        lay.set_mode(tide.TIDE_MODE_COPY_ENGINE)
+        job.reset_outputs()
+        lay.place(job.gathered, job.param_ptrs())
+        torch.cuda.synchronize()
+        gpu_checks.full_check_ag(job)
+        assert job.guards_intact()
 
 
 def _rank_rs_and_pack(job, modes, scale=None):
@@ -285,8 +293,11 @@ FULL = ["llama8b", "llama70b", "moe", "sweep16", "sweep32", "sweep64"]
 def test_full_size_sampled_parity(name):
     """Full-size workloads in the bench's launch configuration (uncapped):
     sampled elements of every (rank, param) against the oracle, every element
-    against a PyTorch fp32 reference; capped mode on the same inputs agrees
-    bit for bit."""
+    against a PyTorch fp32 reference.  Then every other form and mode on the
+    same inputs, each against the oracle (sampled) and the PyTorch reference:
+    single-rank RS, pack, Slot-Reuse staging + staged RS, CTA-capped 64,
+    TMA-staged / TMA-copy modes capped and over every SM, and copy-engine
+    placement."""
     wl = synth.WORKLOADS[name]()
     with tide.Layout(wl.shapes, wl.num_ranks) as lay:
         job = DeviceJob(wl, lay, guard=False)
@@ -297,9 +308,10 @@ def test_full_size_sampled_parity(name):
         gpu_checks.torch_check_rs(job)
         gpu_checks.torch_check_ag(job)
         for r in (0, job.N - 1):
-            outs = [torch.empty(n, dtype=torch.float32, device="cuda") for n in job.shard_numel]
+            outs = [torch.full((n,), float("nan"), dtype=torch.float32, device="cuda") for n in job.shard_numel]
             lay.reduce_scatter_rank(r, job.grad_ptrs(), outs, wl.scale)
             torch.cuda.synchronize()
+            assert gpu_checks.sampled_check_rs(job, seed=10 + r, ranks=[r], outputs={r: outs}) > 0
             for p in range(job.P):
                 assert torch.equal(outs[p].view(torch.int32), job.shards[r][p].view(torch.int32)), (r, p)
             del outs
@@ -308,19 +320,6 @@ def test_full_size_sampled_parity(name):
         torch.cuda.synchronize()
         assert gpu_checks.sampled_check_pack(job) > 0
         del job.pack_src, job.packed
-        # Slot-Reuse: stage every rank, reduce-scatter from the slots; equal
-        # bit for bit to the direct reduce-scatter
-        ref_all = [[s.clone() for s in row] for row in job.shards]
-        job.make_slots()
-        for k in range(job.N):
-            lay.stage([job.grads[k][p] for p in range(job.P)], job.slots[k])
-        lay.reduce_scatter_staged(job.slots, job.shard_ptrs(), wl.scale)
-        torch.cuda.synchronize()
-        for r in range(job.N):
-            for p in range(job.P):
-                assert torch.equal(job.shards[r][p].view(torch.int32), ref_all[r][p].view(torch.int32))
-        del job.slots, ref_all
-        ref = [s.clone() for s in (job.shards[0][0], job.shards[-1][-1])]
 
         def clear_outputs():
             for row in job.shards:
@@ -329,10 +328,22 @@ def test_full_size_sampled_parity(name):
             for prm in job.params:
                 prm.fill_(0x7FA5)  # a bf16 NaN pattern the placement never writes
 
+        # Slot-Reuse: stage every rank, reduce-scatter from the slots
+        job.make_slots()
+        for k in range(job.N):
+            lay.stage([job.grads[k][p] for p in range(job.P)], job.slots[k])
+        clear_outputs()
+        lay.reduce_scatter_staged(job.slots, job.shard_ptrs(), wl.scale)
+        torch.cuda.synchronize()
+        assert gpu_checks.sampled_check_rs(job, seed=1) > 0
+        gpu_checks.torch_check_rs(job)
+        del job.slots
+
         lay.set_mode(tide.TIDE_MODE_CAPPED, 64)
         clear_outputs()
         run(job)
-        assert torch.equal(job.shards[0][0], ref[0]) and torch.equal(job.shards[-1][-1], ref[1])
+        assert gpu_checks.sampled_check_rs(job, seed=2) > 0
+        assert gpu_checks.sampled_check_ag(job, seed=2) > 0
         gpu_checks.torch_check_rs(job)
         gpu_checks.torch_check_ag(job)
         # TMA bulk-staged reduce-scatter and bulk-copy placement, capped and over every SM
@@ -341,8 +352,17 @@ def test_full_size_sampled_parity(name):
             clear_outputs()
             run(job)
             lay.check_device()
+            assert gpu_checks.sampled_check_rs(job, seed=3 + cap) > 0
+            assert gpu_checks.sampled_check_ag(job, seed=3 + cap) > 0
             gpu_checks.torch_check_rs(job)
             gpu_checks.torch_check_ag(job)
+        # copy-engine placement
+        lay.set_mode(tide.TIDE_MODE_COPY_ENGINE)
+        clear_outputs()
+        lay.place(job.gathered, job.param_ptrs())
+        torch.cuda.synchronize()
+        assert gpu_checks.sampled_check_ag(job, seed=5) > 0
+        gpu_checks.torch_check_ag(job)
         del job
         torch.cuda.empty_cache()
 
@@ -552,3 +572,63 @@ def test_cuda_graph_capture_of_the_step(tiny_job):
     lay.close()
     torch.zeros(1, device="cuda").add_(1)  # no CUDA error left behind by the library
     torch.cuda.synchronize()
+
+
+def test_first_call_does_not_wait_for_the_stream():
+    """A layout's first compute calls (device set-up, tile-list and pointer-
+    table uploads) enqueue their copies on the caller's stream and return
+    while that stream is still busy; the results then match the oracle."""
+    import time
+
+    wl = synth.tiny()
+    with tide.Layout(wl.shapes, wl.num_ranks) as lay:
+        job = DeviceJob(wl, lay)
+        s = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            torch.cuda._sleep(3_000_000_000)  # ~1.5 s of device time on s
+        t0 = time.perf_counter()
+        lay.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), wl.scale, stream=s)
+        lay.place(job.gathered, job.param_ptrs(), stream=s)
+        host_s = time.perf_counter() - t0
+        busy = not s.query()
+        s.synchronize()
+        assert busy, "the stream finished before the calls returned; the check says nothing"
+        assert host_s < 0.5, f"first calls held the host for {host_s:.3f} s"
+        gpu_checks.full_check_rs(job)
+        gpu_checks.full_check_ag(job)
+        # a second stream is ordered after the upload made on the first
+        other = DeviceJob(wl, lay, fill=False)
+        other.grads, other.gathered = job.grads, job.gathered
+        s2 = torch.cuda.Stream()
+        lay.reduce_scatter(other.grad_ptrs(), other.shard_ptrs(), wl.scale, stream=s2)
+        s2.synchronize()
+        gpu_checks.full_check_rs(other)
+
+
+def test_first_call_inside_capture_is_refused():
+    """Setting a layout up on the device cannot be captured: the call is
+    refused before it enqueues anything, the capture stays usable, and the
+    same call outside the capture then works."""
+    import warnings
+
+    wl = synth.tiny()
+    with tide.Layout(wl.shapes, wl.num_ranks) as lay:
+        job = DeviceJob(wl, lay)
+        x = torch.zeros(16, device="cuda")
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with warnings.catch_warnings():
+            warnings.simplefilter("ignore")
+            with torch.cuda.graph(g, stream=s):
+                x.add_(1.0)
+                with pytest.raises(tide.TideError) as e:
+                    lay.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), wl.scale, stream=s)
+        assert e.value.status == tide.TIDE_ERR_UNSUPPORTED
+        g.replay()
+        torch.cuda.synchronize()
+        assert float(x[0]) == 1.0
+        lay.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), wl.scale, stream=s)
+        s.synchronize()
+        gpu_checks.full_check_rs(job)

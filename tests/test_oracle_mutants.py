@@ -18,6 +18,10 @@ MUTANTS = {
     "reversed_rank_order": ("for (int32_t k = 0; k < num_ranks; ++k) acc = acc +",
                             "for (int32_t k = num_ranks - 1; k >= 0; --k) acc = acc +"),
     "scale_dropped": ("return acc * scale;", "return acc;"),
+    "acc_starts_neg_zero": ("float acc = 0.0f;", "float acc = -0.0f;"),
+    "flush_subnormal_results": ("return acc * scale;",
+                                "return (acc * scale > -1.17549435e-38f && acc * scale < 1.17549435e-38f) "
+                                "? 0.0f : acc * scale;"),
     "floor_chunk": ("return (d0 + num_ranks - 1) / num_ranks;",
                     "return d0 > 0 && d0 < num_ranks ? 1 : d0 / num_ranks;"),
     "row_off_by_one": ("const int64_t i = (int64_t)r * c + ii; /* row of the full tensor */",

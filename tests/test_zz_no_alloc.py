@@ -13,6 +13,7 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import gpu_checks  # noqa: E402
 import synth  # noqa: E402
 from synth.device import DeviceJob  # noqa: E402
 
@@ -38,11 +39,20 @@ def _shards(job):
     return [s.view(torch.int32).clone() for row in job.shards for s in row]
 
 
+MODES = [("uncapped", tide.TIDE_MODE_UNCAPPED, 0), ("capped3", tide.TIDE_MODE_CAPPED, 3),
+         ("bulk", tide.TIDE_MODE_BULK, 0), ("bulk_cap4", tide.TIDE_MODE_BULK, 4)]
+
+
+@pytest.mark.parametrize("mode", MODES, ids=[m[0] for m in MODES])
 @pytest.mark.parametrize("name", ["tiny", "llama8b"])
-def test_noalloc_matches_regular_entry_point_twice(name):
+def test_noalloc_matches_regular_entry_point_twice(name, mode):
+    """Two calls in a row, each bit-exact against the regular entry point in
+    the same mode and against the CPU oracle (every element of the tiny
+    block; sampled elements of every rank and parameter of the 8B layer)."""
     wl = synth.WORKLOADS[name]()
     stream = torch.cuda.Stream()
     with tide.Layout(wl.shapes, wl.num_ranks) as lay:
+        lay.set_mode(*mode[1:])
         job = DeviceJob(wl, lay, guard=True)
         torch.cuda.synchronize()
         lay.reduce_scatter(job.grad_ptrs(), job.shard_ptrs(), wl.scale, stream)
@@ -57,6 +67,10 @@ def test_noalloc_matches_regular_entry_point_twice(name):
             for a, b in zip(got, want):
                 assert torch.equal(a, b), f"call {call}"  # bit-exact, like every RS comparison
             assert job.guards_intact()
+            if name == "tiny":
+                gpu_checks.full_check_rs(job)
+            else:
+                assert gpu_checks.sampled_check_rs(job, seed=call) > 0
 
 
 def test_noalloc_capped_mode_and_size_limit():
@@ -139,3 +153,20 @@ def test_noalloc_refused_inside_stream_capture():
         graph.replay()
         torch.cuda.synchronize()
         assert float(x[0]) == 1.0
+
+
+def test_noalloc_across_device_reset(tmp_path):
+    """A plain C program (its own process: a device reset would end this
+    one's CUDA context) calls the entry point, resets the device, allocates
+    again (often at the same addresses), refills with other values and calls
+    twice more on the same stream: the library must see the new context,
+    look its array up again and copy, and every shard is exact."""
+    import subprocess
+
+    from test_c_abi_driver import build_reset_driver
+
+    exe = tmp_path / "reset_driver"
+    build_reset_driver(exe)
+    res = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert res.stdout.startswith("ok:"), res.stdout

@@ -39,7 +39,7 @@ COPY_MODES = [("uncapped", tide.TIDE_MODE_UNCAPPED, 0), ("capped2", tide.TIDE_MO
               ("bulk", tide.TIDE_MODE_BULK, 0), ("bulk_cap3", tide.TIDE_MODE_BULK, 3),
               ("copy_engine", tide.TIDE_MODE_COPY_ENGINE, 0)]
 CANARY32 = -0x5A5A5A5B
-CANARY16 = 0x7FA5 - 0x10000
+CANARY16 = 0x7FA5  # fits in int16 as is
 
 
 def dev_u16(a: np.ndarray) -> torch.Tensor:
@@ -109,7 +109,7 @@ def _all_forms(lay, align, n, shps, host, grads_dev, scale, modes, ranks=None):
                 compare_f32(out.t[p], want[r][p], f"{tag} single rank {r} param {p}")
             assert out.intact(), f"{tag} single rank {r}: write outside a shard"
         # Slot-Reuse staging (a bit copy: NaN payloads kept), then the staged RS
-        slots = [torch.full((n * S,), SENTINEL_BF16 - 0x10000, dtype=torch.int16, device="cuda")
+        slots = [torch.full((n * S,), SENTINEL_BF16, dtype=torch.int16, device="cuda")
                  for _ in range(n)]
         for k in range(n):
             lay.stage([grads_dev[k][p] for p in range(P)], slots[k])
@@ -142,7 +142,7 @@ def test_rs_special_values(n, align):
         lay.set_mode(tide.TIDE_MODE_COPY_ENGINE)
         offs, S = oracle.layout(shps, n, align)
         for k in (0, n - 1):
-            slot = torch.full((n * S,), SENTINEL_BF16 - 0x10000, dtype=torch.int16, device="cuda")
+            slot = torch.full((n * S,), SENTINEL_BF16, dtype=torch.int16, device="cuda")
             lay.stage(grads_dev[k], slot)
             torch.cuda.synchronize()
             want = oracle.rs_stage(shps, n, offs, S, host[k], np.full(n * S, SENTINEL_BF16, np.uint16))
@@ -178,7 +178,7 @@ def test_placement_and_staging_keep_nan_payloads(n, align):
             bufs = [torch.full((w.size + 2 * g16,), CANARY16, dtype=torch.int16, device="cuda") for w in want]
             params = [b[g16: g16 + w.size] for b, w in zip(bufs, want)]
             lay.place(gathered, params)
-            slot = torch.full((n * S,), SENTINEL_BF16 - 0x10000, dtype=torch.int16, device="cuda")
+            slot = torch.full((n * S,), SENTINEL_BF16, dtype=torch.int16, device="cuda")
             lay.stage(grads, slot)
             torch.cuda.synchronize()
             lay.check_device()

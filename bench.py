@@ -33,6 +33,7 @@ L2_BYTES = 129 * 1024 * 1024  # GB300; used when the device does not report its 
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
 KERNEL_SRC = os.path.join(ROOT, "layout_aware_collectives_gb300", "csrc", "kernels.cu")
+HBM_LIB = os.path.join(ROOT, "libbench_hbm.so")
 
 
 def parse():
@@ -46,6 +47,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stock", action="store_true")
+    ap.add_argument("--no-hbm-mix", action="store_true")
+    ap.add_argument("--hbm-mix-only", action="store_true",
+                    help="only measure the HBM read/write-mix streams and print them as one JSON line")
+    ap.add_argument("--no-second", action="store_true",
+                    help="skip the second throughput workload (MoE layer after the 70B layer)")
     ap.add_argument("--mode", default="uncapped", choices=["uncapped", "capped", "bulk"],
                     help="kernel mode of the timed step")
     ap.add_argument("--cap", type=int, default=0, help="CTA cap for --mode capped / bulk")
@@ -332,51 +338,34 @@ def emit(out, args):
 
 
 # ---------------------------------------------------------------- GPU arm
-def run_tide(args):
+def smi_device(dev: int) -> str:
+    """nvidia-smi -i takes an index, a UUID or a PCI id: pass the visible entry as is."""
+    visible = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    return visible[dev] if dev < len(visible) else str(dev)
+
+
+def timed_steps(layout, job, wl, stream, K, warmup, world, smi_dev, l2_bytes):
+    """W untimed steps, then K timed steps (one reduce-scatter + one
+    placement each) bracketed by a barrier and a device synchronise, with CUDA
+    events on the launching stream around every launch and nvidia-smi clock
+    samples over the timed region."""
     import torch
 
-    world, rank, local = dist_setup(args.gpus)
     import layout_aware_collectives_gb300 as tide
-    import synth
-    from synth.device import DeviceJob
 
-    dev = torch.cuda.current_device()
-    props = torch.cuda.get_device_properties(dev)
-    wl = synth.WORKLOADS[args.config]()
-    layout = tide.Layout(wl.shapes, wl.num_ranks)
-    job = DeviceJob(wl, layout, guard=False)
-    stream = torch.cuda.Stream()
-    stream.wait_stream(torch.cuda.current_stream())
-    torch.cuda.synchronize()
     gptr = tide.PointerTable(job.grad_ptrs())
     sptr = tide.PointerTable(job.shard_ptrs())
     pptr = tide.PointerTable(job.param_ptrs())
     scale = wl.scale
     rs_bytes, ag_bytes = wl.rs_bytes(), wl.ag_bytes()
-    l2_bytes = getattr(props, "L2_cache_size", 0) or L2_BYTES  # queried; the constant if unknown
     small = (rs_bytes + ag_bytes) < 2 * l2_bytes
     flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device="cuda") if small else None
-
-    step_mode = {"uncapped": tide.TIDE_MODE_UNCAPPED, "capped": tide.TIDE_MODE_CAPPED,
-                 "bulk": tide.TIDE_MODE_BULK}[args.mode]
-    if args.mode == "capped" and args.cap < 1:
-        raise SystemExit("--mode capped needs --cap >= 1")
-    layout.set_mode(step_mode, args.cap)
-
-    def step():
-        layout.reduce_scatter(gptr, sptr, scale, stream)
-        layout.place(job.gathered, pptr, stream)
-
     with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            step()
+        for _ in range(max(3, warmup)):
+            layout.reduce_scatter(gptr, sptr, scale, stream)
+            layout.place(job.gathered, pptr, stream)
     torch.cuda.synchronize()
-
-    K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    # nvidia-smi -i takes an index, a UUID or a PCI id: pass the visible entry as is
-    visible = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
-    smi_dev = visible[dev] if dev < len(visible) else str(dev)
     clocks = ClockSampler(smi_dev)
     clocks.start()
     time.sleep(0.3)
@@ -402,7 +391,49 @@ def run_tide(args):
         step_ms_local = ev[0][0].elapsed_time(ev[K - 1][2]) / K
     else:
         step_ms_local = sum(r + a for r, a in zip(rs_ms, ag_ms)) / K
-    step_ms, value = aggregate(step_ms_local, rs_bytes + ag_bytes, world)
+    del flush
+    return {"step_ms_local": step_ms_local, "rs_ms": rs_ms, "ag_ms": ag_ms, "clocks": clk,
+            "l2": "flushed between steps" if small else
+            f"inputs larger than L2 ({(rs_bytes + ag_bytes) / 1e9:.1f} GB per step)"}
+
+
+def mix_ratio(num_ranks: int) -> int:
+    """Reads per write of the reduce-scatter (2N bytes read per 4 written),
+    rounded to a ratio the HBM-mix probe has."""
+    want = max(1, num_ranks // 2)
+    return min((1, 2, 4, 8, 16), key=lambda r: abs(r - want))
+
+
+def run_tide(args):
+    import torch
+
+    world, rank, local = dist_setup(args.gpus)
+    import layout_aware_collectives_gb300 as tide
+    import synth
+    from synth.device import DeviceJob
+
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    smi_dev = smi_device(dev)
+    l2_bytes = getattr(props, "L2_cache_size", 0) or L2_BYTES  # queried; the constant if unknown
+    wl = synth.WORKLOADS[args.config]()
+    layout = tide.Layout(wl.shapes, wl.num_ranks)
+    job = DeviceJob(wl, layout, guard=False)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    rs_bytes, ag_bytes = wl.rs_bytes(), wl.ag_bytes()
+
+    step_mode = {"uncapped": tide.TIDE_MODE_UNCAPPED, "capped": tide.TIDE_MODE_CAPPED,
+                 "bulk": tide.TIDE_MODE_BULK}[args.mode]
+    if args.mode == "capped" and args.cap < 1:
+        raise SystemExit("--mode capped needs --cap >= 1")
+    layout.set_mode(step_mode, args.cap)
+
+    K = args.steps
+    run = timed_steps(layout, job, wl, stream, K, args.warmup, world, smi_dev, l2_bytes)
+    rs_ms, ag_ms = run["rs_ms"], run["ag_ms"]
+    step_ms, value = aggregate(run["step_ms_local"], rs_bytes + ag_bytes, world)
     rs_avg = statistics.mean(rs_ms)
     ag_avg = statistics.mean(ag_ms)
 
@@ -418,16 +449,9 @@ def run_tide(args):
         "config": {"workload": wl.name, "num_ranks": wl.num_ranks, "num_params": wl.num_params,
                    "psi": wl.psi, "rs_bytes": rs_bytes, "ag_bytes": ag_bytes,
                    "io": "bf16 gradients -> fp32 shards (fp32 sums); bf16 placement (bit copy)",
-                   "l2": "flushed between steps" if small else
-                   f"inputs larger than L2 ({(rs_bytes + ag_bytes) / 1e9:.1f} GB per step)",
+                   "l2": run["l2"],
                    "mode": args.mode + (f" cap {args.cap}" if args.cap else ""),
                    "parallelism": f"replicas x{world}"},
-        "kernels": {
-            "rs": {"ms": round(rs_avg, 4), "GB/s": round(rs_gbs, 1), "frac": round(rs_gbs / peak, 4),
-                   "ms_median": round(statistics.median(rs_ms), 4), "grid": grid_rs, "block": block_rs},
-            "ag": {"ms": round(ag_avg, 4), "GB/s": round(ag_gbs, 1), "frac": round(ag_gbs / peak, 4),
-                   "ms_median": round(statistics.median(ag_ms), 4), "grid": grid_ag, "block": block_ag},
-        },
         "roofline": {"bound": "hbm",
                      "kernel": "tide rs_bulk_kernel" if args.mode == "bulk" else "tide rs_kernel",
                      "achieved": round(rs_gbs, 1),
@@ -435,9 +459,15 @@ def run_tide(args):
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(rs_gbs / peak, 4),
                      "traffic": recorded_traffic(wl.name) if args.mode == "uncapped" else None},
-        "clocks": clk,
+        "clocks": run["clocks"],
         "gpu_launches": 2 * K,
         "device": props.name,
+        "kernels": {
+            "rs": {"ms": round(rs_avg, 4), "GB/s": round(rs_gbs, 1), "frac": round(rs_gbs / peak, 4),
+                   "ms_median": round(statistics.median(rs_ms), 4), "grid": grid_rs, "block": block_rs},
+            "ag": {"ms": round(ag_avg, 4), "GB/s": round(ag_gbs, 1), "frac": round(ag_gbs / peak, 4),
+                   "ms_median": round(statistics.median(ag_ms), 4), "grid": grid_ag, "block": block_ag},
+        },
     }
 
     layout.check_device()  # raises if a bounded device wait ran out during the timed steps
@@ -455,16 +485,129 @@ def run_tide(args):
     if not args.no_interference:
         out["interference"] = run_interference(tide, layout, job, wl, props, smi_dev)
     layout.set_mode(tide.TIDE_MODE_UNCAPPED)
+    layout.close()
+    del job
+    torch.cuda.empty_cache()
+
+    # HBM streams of the reduce-scatter's own read:write mix (the copy peak is 1:1)
+    second = "moe" if args.config != "moe" else "llama70b"
+    ratios = sorted({mix_ratio(wl.num_ranks), mix_ratio(synth.WORKLOADS[second]().num_ranks)})
+    if not args.no_hbm_mix:
+        mix = run_hbm_mix(ratios, smi_dev)
+        out["hbm_mix"] = mix
+        ceiling = mix.get(f"read{mix_ratio(wl.num_ranks)}_write1")
+        if ceiling:
+            out["roofline"]["mix_peak"] = ceiling
+            out["roofline"]["frac_vs_mix"] = round(rs_gbs / ceiling, 4)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, 10.0)
+    if not args.no_second:
+        out[second] = run_second(second, args, world, smi_dev, l2_bytes, peak, out.get("hbm_mix"))
+    if "interference" in out:
+        out["interference_summary"] = interference_summary(out["interference"])
     if rank == 0:
         emit(out, args)
-    layout.close()
     if world > 1:
         import torch.distributed as dist
 
         dist.destroy_process_group()
     return 0
+
+
+def run_second(name, args, world, smi_dev, l2_bytes, peak, mix):
+    """The step on the other throughput workload (MoE layer after the 70B
+    layer, or the reverse), timed the same way, reported compactly."""
+    import torch
+
+    import layout_aware_collectives_gb300 as tide
+    import synth
+    from synth.device import DeviceJob
+
+    wl = synth.WORKLOADS[name]()
+    layout = tide.Layout(wl.shapes, wl.num_ranks)
+    job = DeviceJob(wl, layout, guard=False)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    run = timed_steps(layout, job, wl, stream, args.steps, args.warmup, world, smi_dev, l2_bytes)
+    step_ms, value = aggregate(run["step_ms_local"], wl.rs_bytes() + wl.ag_bytes(), world)
+    rs_gbs = wl.rs_bytes() / (statistics.mean(run["rs_ms"]) * 1e-3) / 1e9
+    ag_gbs = wl.ag_bytes() / (statistics.mean(run["ag_ms"]) * 1e-3) / 1e9
+    res = {"workload": wl.name, "N": wl.num_ranks, "P": wl.num_params, "value_GB/s": round(value, 1),
+           "ms_per_step": round(step_ms, 4), "rs_GB/s": round(rs_gbs, 1), "rs_frac": round(rs_gbs / peak, 4),
+           "ag_GB/s": round(ag_gbs, 1), "ag_frac": round(ag_gbs / peak, 4)}
+    ceiling = (mix or {}).get(f"read{mix_ratio(wl.num_ranks)}_write1")
+    if ceiling:
+        res["rs_frac_vs_mix"] = round(rs_gbs / ceiling, 4)
+    c = run["clocks"]
+    res["clocks"] = {"sm_mhz": c.get("sm_mhz"), "reasons": c.get("reasons"), "samples": c.get("samples")}
+    layout.check_device()
+    layout.close()
+    del job
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_hbm_mix(ratios, smi_dev, out_bytes=1 << 30, reps=10):
+    """HBM rates of streams with a fixed read:write mix (bench_hbm.cu):
+    read-only, write-only, and R reads per write for each R in `ratios`
+    (plus R = 1, a copy); median of `reps` launches by CUDA events, 1 GiB
+    written per launch (R GiB read)."""
+    import ctypes
+
+    import torch
+
+    lib = ctypes.CDLL(HBM_LIB)
+    for f in (lib.hbm_read, lib.hbm_write, lib.hbm_mix):
+        f.restype = ctypes.c_int
+    lib.hbm_read.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    lib.hbm_write.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p]
+    lib.hbm_mix.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    rmax = max([1] + list(ratios))
+    src = torch.empty(max(rmax, 4) * out_bytes, dtype=torch.uint8, device="cuda")
+    dst = torch.empty(out_bytes, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    src.fill_(0x5A)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    sh = stream.cuda_stream
+
+    def rate(launch, nbytes):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                assert launch() == 0
+            ms = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                assert launch() == 0
+                e1.record(stream)
+                ms.append((e0, e1))
+        torch.cuda.synchronize()
+        t = statistics.median(a.elapsed_time(b) for a, b in ms)
+        return round(nbytes / (t * 1e-3) / 1e9, 1)
+
+    clocks = ClockSampler(smi_dev)
+    clocks.start()
+    time.sleep(0.2)
+    t0 = time.time()
+    rd_bytes = src.numel()
+    wr_bytes = 4 * out_bytes
+    res = {"kernel": "bench_hbm.cu: one 512-thread CTA per tile, 16-byte ld.global.nc / st.global.cs",
+           "read_only": rate(lambda: lib.hbm_read(src.data_ptr(), rd_bytes, sink.data_ptr(), sh), rd_bytes),
+           "write_only": rate(lambda: lib.hbm_write(src.data_ptr(), wr_bytes, 7, sh), wr_bytes)}
+    for r in sorted({1} | set(ratios)):
+        res[f"read{r}_write1"] = rate(lambda r=r: lib.hbm_mix(src.data_ptr(), dst.data_ptr(), out_bytes, r, sh),
+                                      (r + 1) * out_bytes)
+    t1 = time.time()
+    rd, wr = res["read_only"], res["write_only"]
+    # the rate a stream with read fraction f would reach if reads ran at the
+    # read-only rate and writes at the write-only rate, one after the other
+    res["bound_from_read_and_write_rates"] = {
+        f"read{r}_write1": round(1.0 / ((r / (r + 1)) / rd + (1 / (r + 1)) / wr), 1) for r in sorted({1} | set(ratios))}
+    res["clocks"] = clocks.stop(t0, t1)
+    del src, dst, sink
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_next_ops(tide, layout, job, wl, stream, reps=20):
@@ -750,13 +893,22 @@ def run_e2e(tide, layout, job, wl, stream, K, world):
     return out
 
 
-def run_interference(tide, layout, job, wl, props, smi_dev):
+def run_interference(tide, layout, job, wl, props, smi_dev, repeats=3, window_s=0.3):
     """Slowdown of a bf16 8192^3 GEMM on one stream while the reduce-scatter
     (or placement) loops on another, per mode; the op's bandwidth during the
     GEMM window and its SM.time.  Modes marked `_lowprio` put the GEMM on a
     high-priority stream and the op on a low-priority one: the block
     scheduler then dispatches pending GEMM CTAs first, and the op's
-    one-CTA-per-tile launches fill whatever the GEMM leaves."""
+    one-CTA-per-tile launches fill whatever the GEMM leaves.
+
+    Per mode, `repeats` pairs of windows of at least `window_s` seconds each
+    (several nvidia-smi samples per window): the GEMMs alone, then the same
+    number of GEMMs beside the op.  Reported: the median slowdown and its
+    range over the repeats, and the slowdown in GEMM clock cycles (window
+    time x median SM clock of the window), which takes out the part a lower
+    clock under the shared power cap explains."""
+    import math
+
     import torch
 
     n = 8192
@@ -770,37 +922,61 @@ def run_interference(tide, layout, job, wl, props, smi_dev):
     gptr = tide.PointerTable(job.grad_ptrs())
     sptr = tide.PointerTable(job.shard_ptrs())
     pptr = tide.PointerTable(job.param_ptrs())
-    reps = 8
 
-    def gemm_events(sg):
+    def gemm_window(sg, count):
+        """Events around `count` back-to-back GEMMs on sg (not synchronised)."""
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(sg):
             e0.record(sg)
-            for _ in range(reps):
+            for _ in range(count):
                 torch.matmul(a, b, out=c)
             e1.record(sg)
         return e0, e1
 
-    def gemm_alone(sg):
-        for _ in range(3):
-            gemm_events(sg)
+    def gemm_alone(sg, count):
+        e0, e1 = gemm_window(sg, count)
         torch.cuda.synchronize()
-        t = []
-        for _ in range(5):
-            e0, e1 = gemm_events(sg)
-            torch.cuda.synchronize()
-            t.append(e0.elapsed_time(e1) / reps)
-        return statistics.median(t)
+        return e0.elapsed_time(e1) / count
 
-    t0 = gemm_alone(streams[False][0])
-    t0_hi = gemm_alone(streams[True][0])
+    def concurrent(sg, sr, op, count, launches, nbytes):
+        """`launches` op launches on sr (an event pair each), then `count`
+        GEMMs on sg once the op loop runs: GEMM ms, bytes the op moved inside
+        the GEMM window, mean op launch ms."""
+        evs = []
+        with torch.cuda.stream(sr):
+            for _ in range(launches):
+                x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                x0.record(sr)
+                op()
+                x1.record(sr)
+                evs.append((x0, x1))
+        time.sleep(0.002)
+        e0, e1 = gemm_window(sg, count)
+        torch.cuda.synchronize()
+        window = e0.elapsed_time(e1)
+        moved = 0.0
+        for x0, x1 in evs:
+            st, en = e0.elapsed_time(x0), e0.elapsed_time(x1)
+            if en > st:
+                moved += nbytes * max(0.0, min(en, window) - max(st, 0.0)) / (en - st)
+        return window / count, moved / (window * 1e-3) / 1e9, evs[0][0].elapsed_time(evs[-1][1]) / launches
+
+    for prio in (False, True):
+        for _ in range(3):
+            gemm_window(streams[prio][0], 8)
+    torch.cuda.synchronize()
+    t0 = statistics.median(gemm_alone(streams[False][0], 8) for _ in range(5))
+    t0_hi = statistics.median(gemm_alone(streams[True][0], 8) for _ in range(5))
+    count = max(8, math.ceil(window_s * 1e3 / t0))
     flops = 2 * n ** 3
     res = {"gemm": f"bf16 {n}x{n}x{n} torch.matmul", "gemm_ms_alone": round(t0, 4),
            "gemm_tflops_alone": round(flops / (t0 * 1e-3) / 1e12, 1),
            "gemm_ms_alone_high_priority": round(t0_hi, 4),
            "stream_priorities": {"least": least, "greatest": greatest},
+           "windows": f"{repeats} repeats per mode of {count} GEMMs alone, then {count} GEMMs beside the op",
            "op_GB/s_during_gemm": "bytes the op moved inside the GEMM window (each launch weighted by "
                                   "its overlap with the window) / window length",
+           "slowdown_cycles": "slowdown of GEMM time x median SM MHz of its window (clock-normalised)",
            "modes": []}
     U, C, B, CE = (tide.TIDE_MODE_UNCAPPED, tide.TIDE_MODE_CAPPED, tide.TIDE_MODE_BULK,
                    tide.TIDE_MODE_COPY_ENGINE)
@@ -816,9 +992,6 @@ def run_interference(tide, layout, job, wl, props, smi_dev):
     time.sleep(0.2)
     for kind, name, mode, cap, prio in modes:
         sg, sr = streams[prio]
-        w0 = time.time()
-        # the GEMM's own time drifts with its power state: re-measure it beside each mode
-        base = gemm_alone(sg)
         layout.set_mode(mode, cap)
         if kind == "rs":
             def op():
@@ -838,44 +1011,49 @@ def run_interference(tide, layout, job, wl, props, smi_dev):
             for _ in range(3):
                 op()
             x1.record(sr)
-            torch.cuda.synchronize()
-            alone_ms = x0.elapsed_time(x1) / 3
-            # enough launches to cover the GEMM window twice over, one event pair each
-            count = max(2, int(2 * reps * base / max(alone_ms, 1e-3)) + 2)
-            evs = []
-            for _ in range(count):
-                x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                x0.record(sr)
-                op()
-                x1.record(sr)
-                evs.append((x0, x1))
-        # start the GEMMs once the op loop is running
-        time.sleep(0.002)
-        e0, e1 = gemm_events(sg)
         torch.cuda.synchronize()
-        window = e0.elapsed_time(e1)
-        t1 = window / reps
-        moved = 0.0
-        for x0, x1 in evs:
-            st, en = e0.elapsed_time(x0), e0.elapsed_time(x1)
-            if en > st:
-                moved += nbytes * max(0.0, min(en, window) - max(st, 0.0)) / (en - st)
-        loop_ms = evs[0][0].elapsed_time(evs[-1][1]) / count
-        w1 = time.time()
+        alone_ms = x0.elapsed_time(x1) / 3
+        # a short probe sizes the op loop of the long windows: it must cover the GEMMs
+        base_p = gemm_alone(sg, 8)
+        t1_p, _, _ = concurrent(sg, sr, op, 8, max(2, int(2 * 8 * base_p * 5 / max(alone_ms, 1e-3)) + 2), nbytes)
+        reps = []
+        for _ in range(repeats):
+            h0 = time.time()
+            base = gemm_alone(sg, count)
+            h1 = time.time()
+            launches = max(2, math.ceil(1.3 * count * t1_p / max(alone_ms, 1e-3)) + 2)
+            t1, during, loop_ms = concurrent(sg, sr, op, count, launches, nbytes)
+            h2 = time.time()
+            cb, cc = sampler.summary(h0, h1), sampler.summary(h1, h2)
+            r = {"gemm_ms_alone": base, "gemm_ms_concurrent": t1, "during": during, "loop_ms": loop_ms,
+                 "slowdown": 100.0 * (t1 / base - 1.0), "mhz_alone": cb["sm_mhz"], "mhz_concurrent": cc["sm_mhz"],
+                 "samples": (cb.get("samples") or 0) + (cc.get("samples") or 0),
+                 "reasons": sorted(set(cb["reasons"]) | set(cc["reasons"]))}
+            if cb["sm_mhz"] and cc["sm_mhz"]:
+                r["slowdown_cycles"] = 100.0 * (t1 * cc["sm_mhz"] / (base * cb["sm_mhz"]) - 1.0)
+            reps.append(r)
         grid, _ = layout.launch_shape(opname)
         sm_used = min(grid, props.multi_processor_count) if grid else 0
+        sl = [r["slowdown"] for r in reps]
+        cyc = [r["slowdown_cycles"] for r in reps if "slowdown_cycles" in r]
+        med = lambda xs, k=None: statistics.median(xs) if xs else None  # noqa: E731
         res["modes"].append({
             "op": kind, "mode": name, "grid": grid,
             "priority": "gemm high, op low" if prio else "equal",
             "op_ms_alone": round(alone_ms, 4),
             "op_GB/s_alone": round(nbytes / (alone_ms * 1e-3) / 1e9, 1),
-            "op_ms_concurrent": round(loop_ms, 4),
-            "op_GB/s_during_gemm": round(moved / (window * 1e-3) / 1e9, 1),
-            "gemm_ms_alone": round(base, 4),
-            "gemm_ms_concurrent": round(t1, 4),
-            "gemm_slowdown_pct": round(100.0 * (t1 / base - 1.0), 2),
+            "op_ms_concurrent": round(med([r["loop_ms"] for r in reps]), 4),
+            "op_GB/s_during_gemm": round(med([r["during"] for r in reps]), 1),
+            "gemm_ms_alone": round(med([r["gemm_ms_alone"] for r in reps]), 4),
+            "gemm_ms_concurrent": round(med([r["gemm_ms_concurrent"] for r in reps]), 4),
+            "gemm_slowdown_pct": round(med(sl), 2),
+            "gemm_slowdown_pct_range": [round(min(sl), 2), round(max(sl), 2)],
+            "gemm_slowdown_cycles_pct": round(med(cyc), 2) if cyc else None,
             "sm_ms": round(alone_ms * sm_used, 2),
-            "clocks": sampler.summary(w0, w1),
+            "clocks": {"sm_mhz_alone": med([r["mhz_alone"] for r in reps if r["mhz_alone"]]),
+                       "sm_mhz_concurrent": med([r["mhz_concurrent"] for r in reps if r["mhz_concurrent"]]),
+                       "samples": sum(r["samples"] for r in reps),
+                       "reasons": sorted(set().union(*[r["reasons"] for r in reps]))},
         })
     res["clocks"] = sampler.stop()
     layout.set_mode(tide.TIDE_MODE_UNCAPPED, 0)
@@ -883,10 +1061,36 @@ def run_interference(tide, layout, job, wl, props, smi_dev):
     return res
 
 
+def interference_summary(res):
+    """One short row per mode, for the end of the JSON line."""
+    short = {"sw_power_cap": "pcap", "hw_slowdown": "HW", "hw_thermal_slowdown": "HWT",
+             "sw_thermal_slowdown": "SWT"}
+    rows = []
+    for m in res["modes"]:
+        if m["op"] == "ag" and m["mode"] not in ("uncapped_lowprio", "copy_engine"):
+            continue
+        c = m["clocks"]
+        rows.append([f"{m['op']} {m['mode']}", m["grid"], m["gemm_slowdown_pct"], m["gemm_slowdown_pct_range"],
+                     m["gemm_slowdown_cycles_pct"], round(m["op_GB/s_during_gemm"]),
+                     round(c["sm_mhz_concurrent"] or 0), round(c["sm_mhz_alone"] or 0), c["samples"],
+                     "+".join(short.get(x, x) for x in c["reasons"])])
+    return {"gemm_ms_alone": res["gemm_ms_alone"],
+            "cols": "mode, grid, GEMM slowdown % (median), [min, max] over repeats, slowdown % in cycles, "
+                    "op GB/s during GEMM, SM MHz beside op, SM MHz GEMM alone, clock samples, reasons",
+            "rows": rows}
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.hbm_mix_only:
+        import torch
+
+        torch.cuda.set_device(0)
+        emit({"hbm_mix": run_hbm_mix([1, 2, 4, 8, 16], smi_device(0)), "device": torch.cuda.get_device_name(0),
+              "peak_copy_gbs": measured_peaks()[0]}, args)
+        return 0
     return run_tide(args)
 
 

@@ -64,14 +64,16 @@
  *    such graphs are no longer replayed.
  *  - A failed CUDA call is reported through the status and cleared from the
  *    runtime's per-thread last error.
- *  - Next to compute kernels, enqueue the calls on a low-priority stream
+ *  - Next to compute kernels, either cap the CTAs (TIDE_MODE_CAPPED) or
+ *    enqueue the calls on a low-priority stream
  *    (cudaStreamCreateWithPriority) and the compute on a higher-priority
  *    one: outside the capped mode every launch is one short-lived CTA per
  *    tile, so the block scheduler dispatches the compute kernel's pending
- *    CTAs first and the collective fills what it leaves (on GB300 a bf16
- *    8192^3 GEMM then loses about what 8-16 capped CTAs would cost it,
- *    -2% to +11%, while the reduce-scatter still moves ~2.4 TB/s beside it,
- *    2-3.5x what those capped modes move).
+ *    CTAs first and the collective fills what it leaves.  Measured on GB300
+ *    beside a loop of bf16 8192^3 GEMMs over 0.3 s windows (power-capped
+ *    clock): equal priority +284% GEMM time; low priority +9.6% with the
+ *    reduce-scatter moving 0.33 TB/s, about what 8 capped CTAs cost (+8.8%,
+ *    0.38 TB/s); capped 16 / 32 / 64 CTAs +13% / +24% / +52%.
  *  - A layout may be used from several host threads (calls are serialised
  *    internally).  Calls on different streams that write the same output
  *    buffers race, as any two kernels would.

@@ -110,7 +110,8 @@ typedef enum {
   TIDE_ERR_UNSUPPORTED = 3,
   TIDE_ERR_CUDA = 4,
   TIDE_ERR_TIMEOUT = 5, /* a bounded device wait ran out (tide_layout_check_device) */
-  TIDE_ERR_OUT_OF_MEMORY = 6
+  TIDE_ERR_OUT_OF_MEMORY = 6,
+  TIDE_ERR_RANGE = 7    /* debug build: a kernel skipped an out-of-range tile (tide_layout_check_device) */
 } tide_status_t;
 
 typedef enum {
@@ -378,7 +379,12 @@ TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t layout, const 
  * the layout's device error word: TIDE_ERR_TIMEOUT if, since the last check,
  * a bounded wait inside a bulk-copy (TMA engine) kernel of this layout ran
  * out — the kernel then abandoned its remaining copies, so the outputs of
- * that call are incomplete — else TIDE_OK.  The wait bound is 2 s.
+ * that call are incomplete — else TIDE_OK.  The wait bound is 2 s.  In a
+ * debug build (see tide_build_info) every kernel first checks each tile it
+ * fetches against the extents of its call's buffers (the test
+ * tide_layout_check_tiles applies); a tile that fails is skipped and this
+ * call returns TIDE_ERR_RANGE (taking precedence over a timeout).  The
+ * no-allocation entry point has no device error word and is not checked.
  */
 TIDE_API tide_status_t tide_layout_check_device(tide_layout_t layout);
 
@@ -390,6 +396,27 @@ TIDE_API tide_status_t tide_layout_check_device(tide_layout_t layout);
  * without faulting or hanging a GPU.
  */
 TIDE_API tide_status_t tide_layout_set_test_stall(tide_layout_t layout, int64_t ns);
+
+/*
+ * Host check of a tile list against the layout's extents, with the test the
+ * kernels of a debug build apply to every tile they fetch.  `rows` holds
+ * `count` tiles of `op` as tide_layout_tiles writes them (6 int64: param,
+ * rank, src_offset, dst_offset, length, flags).  A tile passes when its
+ * parameter and rank exist, its offsets and length are non-negative, its
+ * source run (unless it is a zero-fill tile) and its destination run lie
+ * inside their buffers — the gradient / parameter storage of the parameter
+ * (d0*inner elements), its fp32 shard (c*inner), or one rank-major buffer
+ * (N*S) — its flags are known, zero-fill tiles appear only in reduce-scatter
+ * lists, and a vector tile's offsets have the element alignment its 16-byte
+ * accesses need.  *first_bad receives the index of the first failing tile,
+ * or -1 when all pass.  Host-only.
+ */
+TIDE_API tide_status_t tide_layout_check_tiles(tide_layout_t layout, tide_op_t op, const int64_t* rows,
+                                               int64_t count, int64_t* first_bad);
+
+/* "release", or "debug: device range checks" for the library built with
+ * TIDE_DEBUG=1 (libtide_debug.so). */
+TIDE_API const char* tide_build_info(void);
 
 /* Static description of a status code. */
 TIDE_API const char* tide_status_string(tide_status_t status);

@@ -76,6 +76,21 @@ __device__ __forceinline__ void add8(float (&acc)[8], const uint4& v) {
   acc[7] = __fadd_rn(acc[7], bf16_hi(v.w));
 }
 
+// Debug builds: false when the tile addresses anything outside the buffers of
+// its call (tile_in_range); `reporter` then sets the range bit of the error
+// word, and the caller skips the tile.  Release builds: always true.
+__device__ __forceinline__ bool tile_ok(const Tile& t, int kind, const Extents& e, int* err, bool reporter) {
+#if TIDE_DEBUG
+  if (e.grad_numel && !tile_in_range(t, kind, e)) {
+    if (reporter && err) atomicOr(err, kDevErrRange);
+    return false;
+  }
+#else
+  (void)t, (void)kind, (void)e, (void)err, (void)reporter;
+#endif
+  return true;
+}
+
 // ---------------------------------------------------------------- reduce-scatter
 // One group of G ranks starting at rank k0: issue all G*V loads, then add
 // them in ascending rank order.  FULL means k0 + G <= N is known.
@@ -116,6 +131,7 @@ __global__ void __launch_bounds__(THREADS, TIDE_RS_MIN_BLOCKS) rs_kernel(RsArgs 
   int buf = 0;
   for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
+    if (!tile_ok(tile, a.kind, a.ext, a.err, threadIdx.x == 0)) continue;  // uniform over the CTA
     float* __restrict__ out = a.stab[(int64_t)tile.r * a.num_params + tile.p] + tile.dst;
 
     if (tile.flags & kTileZero) {  // padding rows of the shard
@@ -195,6 +211,7 @@ __global__ void __launch_bounds__(THREADS) ag_kernel(AgArgs a) {
   for (int64_t t = (int64_t)blockIdx.x * WORKERS + (int)threadIdx.x / WT; t < a.num_tiles;
        t += (int64_t)gridDim.x * WORKERS) {
     const Tile tile = a.tiles[t];
+    if (!tile_ok(tile, kKindCopy, a.ext, a.err, lane == 0)) continue;  // uniform over the group
     const uint16_t* __restrict__ src;
     uint16_t* __restrict__ dst;
     if constexpr (TO_BUF) {
@@ -335,6 +352,10 @@ __device__ __forceinline__ bool next_chunk(Cursor& c, const AgArgs& a, const voi
     if (c.t >= a.num_tiles) return false;
     const Tile tile = a.tiles[c.t];
     c.off = 0;
+    if (!tile_ok(tile, kKindCopy, a.ext, nullptr, false)) {  // reported by the plain-copy pass
+      c.bytes = 0;
+      continue;
+    }
     c.bytes = (tile.flags & kTileVec) ? (uint64_t)(tile.len & ~7) * 2u : 0u;
     const unsigned char* b = (const unsigned char*)(a.buf + tile.src);
     const unsigned char* q = (const unsigned char*)(a.ptab[tile.p] + tile.dst);
@@ -363,6 +384,7 @@ __global__ void __launch_bounds__(32) ag_bulk_kernel(AgArgs a) {
   // plain-copy parts: unaligned runs, and the < 8 element tails of vector runs
   for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
+    if (!tile_ok(tile, kKindCopy, a.ext, a.err, threadIdx.x == 0)) continue;
     const uint16_t* b = a.buf + tile.src;
     uint16_t* q = a.ptab[tile.p] + tile.dst;
     const uint16_t* src = TO_BUF ? q : b;
@@ -375,7 +397,7 @@ __global__ void __launch_bounds__(32) ag_bulk_kernel(AgArgs a) {
   for (int s = 0; s <= S; ++s) bulk::mbar_init(&full[s], 1);
   bulk::fence_mbar_init();
   if (a.test_stall_ns) {  // a barrier nothing arrives on: the wait must run out
-    if (!bulk::mbar_wait(&full[S], 0, a.test_stall_ns)) atomicExch(a.err, kDevErrTimeout);
+    if (!bulk::mbar_wait(&full[S], 0, a.test_stall_ns)) atomicOr(a.err, kDevErrTimeout);
     return;
   }
 
@@ -393,7 +415,7 @@ __global__ void __launch_bounds__(32) ag_bulk_kernel(AgArgs a) {
   for (int64_t j = 0; j < issued; ++j) {
     const int s = (int)(j % S);
     if (!bulk::mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.timeout_ns)) {
-      atomicExch(a.err, kDevErrTimeout);
+      atomicOr(a.err, kDevErrTimeout);
       for (int64_t k = j; k < issued; ++k)  // loads that may still land in this CTA's shared memory
         bulk::mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), a.timeout_ns);
       bulk::wait_all();
@@ -478,7 +500,7 @@ __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
   __syncthreads();
 
   if (a.test_stall_ns) {  // wait on a phase nothing completes: must run out
-    if (threadIdx.x == 0 && !bulk::mbar_wait(&full[0], 0, a.test_stall_ns)) atomicExch(a.err, kDevErrTimeout);
+    if (threadIdx.x == 0 && !bulk::mbar_wait(&full[0], 0, a.test_stall_ns)) atomicOr(a.err, kDevErrTimeout);
     return;
   }
 
@@ -487,6 +509,7 @@ __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
     int64_t j = 0;
     for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
       const Tile tile = a.tiles[t];
+      if (!tile_ok(tile, a.kind, a.ext, a.err, false)) continue;  // the consumers report it
       if ((tile.flags & kTileZero) || !(tile.flags & kTileVec)) continue;
       const int vec = tile.len & ~7;
       if (vec == 0) continue;
@@ -500,7 +523,7 @@ __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
           int ok = lane == 0 ? (int)bulk::mbar_wait(&empty[s], (uint32_t)(((j / S) + 1) & 1), a.timeout_ns) : 0;
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) {
-            if (lane == 0) atomicExch(a.err, kDevErrTimeout);
+            if (lane == 0) atomicOr(a.err, kDevErrTimeout);
             // loads issued into the ring may still land: wait (bounded) for them
             for (int64_t k = (j >= S ? j - S : 0); k < j; ++k)
               if (lane == 0) bulk::mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), a.timeout_ns);
@@ -522,6 +545,7 @@ __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
   int64_t j = 0;
   for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
+    if (!tile_ok(tile, a.kind, a.ext, a.err, cid == 0)) continue;  // the producer skips it too
     float* __restrict__ out = a.stab[(int64_t)tile.r * a.num_params + tile.p] + tile.dst;
     if (tile.flags & kTileZero) {
       for (int e = cid; e < tile.len; e += kRsBulkConsumers) out[e] = 0.f;
@@ -536,7 +560,7 @@ __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
       const int n = min(E, vec - off);
       const int s = (int)(j % S);
       if (!bulk::mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.timeout_ns)) {
-        atomicExch(a.err, kDevErrTimeout);
+        atomicOr(a.err, kDevErrTimeout);
         return;
       }
       const unsigned char* st = rs_smem + (size_t)s * stage_bytes;
@@ -584,6 +608,7 @@ __global__ void __launch_bounds__(THREADS) pack_kernel(PackArgs a) {
   for (int64_t t = (int64_t)blockIdx.x * WORKERS + (int)threadIdx.x / WT; t < a.num_tiles;
        t += (int64_t)gridDim.x * WORKERS) {
     const Tile tile = a.tiles[t];
+    if (!tile_ok(tile, kKindPack, a.ext, a.err, lane == 0)) continue;  // uniform over the group
     const float* __restrict__ src = a.stab[(int64_t)tile.r * a.num_params + tile.p] + tile.src;
     uint16_t* __restrict__ dst = a.buf + tile.dst;
     int e0 = 0;

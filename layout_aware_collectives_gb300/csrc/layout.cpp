@@ -348,6 +348,42 @@ tide_status_t tide_layout_tiles(tide_layout_t l, tide_op_t op, int64_t* rows, in
   return TIDE_OK;
 }
 
+tide_status_t tide_layout_check_tiles(tide_layout_t l, tide_op_t op, const int64_t* rows, int64_t count,
+                                      int64_t* first_bad) {
+  if (!l || !first_bad || count < 0 || (count > 0 && !rows))
+    return set_error(TIDE_ERR_INVALID_ARG, "NULL argument or negative count");
+  if (op < TIDE_OP_RS || op > TIDE_OP_STAGED_RS) return set_error(TIDE_ERR_INVALID_ARG, "unknown op");
+  const int kind = op == TIDE_OP_RS          ? tide::kKindRs
+                   : op == TIDE_OP_STAGED_RS ? tide::kKindStagedRs
+                   : op == TIDE_OP_PACK      ? tide::kKindPack
+                                             : tide::kKindCopy;  // placement and staging
+  std::vector<int64_t> numel(l->num_params);
+  for (int32_t p = 0; p < l->num_params; ++p) numel[p] = l->d0[p] * l->inner[p];
+  tide::Extents e;
+  e.grad_numel = numel.data();
+  e.shard_numel = l->shard_numel.data();
+  e.buf_numel = l->block_numel * l->num_ranks;
+  e.num_params = l->num_params;
+  e.num_ranks = l->num_ranks;
+  *first_bad = -1;
+  auto fits32 = [](int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; };
+  for (int64_t i = 0; i < count; ++i) {
+    const int64_t* r = rows + 6 * i;
+    bool ok = fits32(r[0]) && fits32(r[1]) && fits32(r[4]) && r[5] >= 0 && r[5] <= (int64_t)UINT32_MAX;
+    if (ok) {
+      const tide::Tile t{r[2], r[3], (int32_t)r[4], (int32_t)r[0], (int32_t)r[1], (uint32_t)r[5]};
+      ok = tide::tile_in_range(t, kind, e);
+    }
+    if (!ok) {
+      *first_bad = i;
+      break;
+    }
+  }
+  return TIDE_OK;
+}
+
+const char* tide_build_info(void) { return TIDE_DEBUG ? "debug: device range checks" : "release"; }
+
 const char* tide_status_string(tide_status_t s) {
   switch (s) {
     case TIDE_OK: return "TIDE_OK";
@@ -357,6 +393,7 @@ const char* tide_status_string(tide_status_t s) {
     case TIDE_ERR_CUDA: return "TIDE_ERR_CUDA: CUDA runtime error";
     case TIDE_ERR_TIMEOUT: return "TIDE_ERR_TIMEOUT: bounded device wait expired";
     case TIDE_ERR_OUT_OF_MEMORY: return "TIDE_ERR_OUT_OF_MEMORY: allocation failed";
+    case TIDE_ERR_RANGE: return "TIDE_ERR_RANGE: a debug-build kernel skipped an out-of-range tile";
   }
   return "unknown tide_status_t";
 }

@@ -79,6 +79,8 @@ void release_device(tide_layout_s* l) {
   }
   if (l->d_err) cudaFree(l->d_err);
   l->d_err = nullptr;
+  if (l->d_extents) cudaFree(l->d_extents);
+  l->d_extents = nullptr;
   if (l->tables_ev) {
     cudaEventSynchronize(l->tables_ev);  // the upload reads the staging
     cudaEventDestroy(l->tables_ev);
@@ -139,11 +141,13 @@ tide_status_t bind_device(tide_layout_s* l, int dev, cudaStream_t stream) {
                 {&l->ag_tiles, &l->d_ag_tiles, "placement tile list"},
                 {&l->pk_tiles, &l->d_pk_tiles, "pack tile list"},
                 {&l->st_tiles, &l->d_st_tiles, "staged reduce-scatter tile list"}};
-  // One pinned staging buffer for the four lists: the copies are then
-  // asynchronous (a pageable source would make the host wait for the stream).
+  // One pinned staging buffer for the four lists and the extents: the copies
+  // are then asynchronous (a pageable source would make the host wait for
+  // the stream).
+  const size_t P = (size_t)l->num_params;
   size_t total = 0;
   for (auto& t : lists) total += t.host->size();
-  TIDE_CUDA(cudaMallocHost(&l->h_tile_staging, sizeof(Tile) * std::max<size_t>(1, total)),
+  TIDE_CUDA(cudaMallocHost(&l->h_tile_staging, sizeof(Tile) * total + 2 * sizeof(int64_t) * std::max<size_t>(1, P)),
             "cudaMallocHost(tile-list staging)");
   Tile* staged = (Tile*)l->h_tile_staging;
   for (auto& t : lists) {
@@ -156,6 +160,17 @@ tide_status_t bind_device(tide_layout_s* l, int dev, cudaStream_t stream) {
       staged += t.host->size();
     }
   }
+  // extents the debug build's kernels check every tile against
+  int64_t* ext = (int64_t*)staged;
+  for (size_t p = 0; p < P; ++p) {
+    ext[p] = l->d0[p] * l->inner[p];
+    ext[P + p] = l->shard_numel[p];
+  }
+  TIDE_CUDA(cudaMalloc((void**)&l->d_extents, 2 * sizeof(int64_t) * std::max<size_t>(1, P)),
+            "cudaMalloc(extents)");
+  if (P)
+    TIDE_CUDA(cudaMemcpyAsync(l->d_extents, ext, 2 * sizeof(int64_t) * P, cudaMemcpyHostToDevice, stream),
+              "extents");
   TIDE_CUDA(cudaMalloc((void**)&l->d_err, sizeof(int)), "cudaMalloc(error word)");
   TIDE_CUDA(cudaMemsetAsync(l->d_err, 0, sizeof(int), stream), "cudaMemsetAsync(error word)");
   TIDE_CUDA(cudaEventCreateWithFlags(&l->tables_ev, cudaEventDisableTiming), "cudaEventCreate");
@@ -355,6 +370,16 @@ tide_status_t copy_engine(tide_layout_s* l, uint16_t* buf, uint16_t* const* para
 
 }  // namespace
 
+Extents extents_of(const tide_layout_s* l) {
+  Extents e;
+  e.grad_numel = l->d_extents;
+  e.shard_numel = l->d_extents + l->num_params;
+  e.buf_numel = l->block_numel * l->num_ranks;
+  e.num_params = l->num_params;
+  e.num_ranks = l->num_ranks;
+  return e;
+}
+
 int grid_of(const tide_layout_s* l, int64_t tiles, int per_sm) {
   return grid_for(tiles, l->mode, l->cta_cap, l->num_sms, per_sm);
 }
@@ -391,6 +416,8 @@ tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, cons
   a.err = l->d_err;
   a.timeout_ns = TIDE_BULK_TIMEOUT_NS;
   a.test_stall_ns = (uint64_t)l->test_stall_ns;
+  a.ext = extents_of(l);
+  a.kind = staged ? kKindStagedRs : kKindRs;
   // TMA-staged kernel: a stage holds one chunk's N rank slices.  Measured on
   // GB300, slices of 4 KiB over every SM (8 KiB when capped) keep the
   // bulk-copy engine busy and smaller ones do not, so the stage grows with N
@@ -445,6 +472,7 @@ cudaError_t launch_copy(tide_layout_s* l, AgArgs& a, bool to_buf, cudaStream_t s
   a.err = l->d_err;
   a.timeout_ns = TIDE_BULK_TIMEOUT_NS;
   a.test_stall_ns = (uint64_t)l->test_stall_ns;
+  a.ext = extents_of(l);
   const bool capped = l->mode == TIDE_MODE_CAPPED;
   if (l->mode == TIDE_MODE_BULK)
     return launch_ag_bulk(a, grid_of(l, a.num_tiles, 0), to_buf, stream);
@@ -608,6 +636,8 @@ tide_status_t tide_ag_pack_bf16(tide_layout_t l, int32_t rank, const float* cons
   a.stab = (const float* const*)slot->d_table;
   a.buf = gathered;
   a.num_params = P;
+  a.err = l->d_err;
+  a.ext = extents_of(l);
   cudaError_t e = launch_pack(a, grid_of(l, t1 - t0, 0), l->mode == TIDE_MODE_CAPPED, stream);
   if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
   return mark_used(l, slot, stream);
@@ -687,6 +717,10 @@ tide_status_t tide_layout_check_device(tide_layout_t l) {
   TIDE_CUDA(cudaMemcpy(&v, l->d_err, sizeof v, cudaMemcpyDeviceToHost), "read of the error word");
   if (v == 0) return TIDE_OK;
   TIDE_CUDA(cudaMemset(l->d_err, 0, sizeof(int)), "reset of the error word");
+  if (v & kDevErrRange)
+    return set_error(TIDE_ERR_RANGE, std::string("a kernel of the debug build skipped a tile that addresses memory "
+                                                 "outside its call's buffers") +
+                                         (v & kDevErrTimeout ? "; a bounded wait also ran out" : ""));
   return set_error(TIDE_ERR_TIMEOUT, "a bounded wait in a bulk-copy kernel ran out; its copies were abandoned");
 }
 

@@ -29,6 +29,57 @@ static_assert(sizeof(Tile) == 32, "Tile is 32 bytes");
 constexpr uint32_t kTileZero = 1u;  // RS only: write +0.0f (padding rows)
 constexpr uint32_t kTileVec = 2u;   // source and destination allow 16-byte vectors
 
+// Debug builds (-DTIDE_DEBUG=1) check every tile a kernel fetches against the
+// extents of the buffers of its call before touching memory.
+#ifndef TIDE_DEBUG
+#define TIDE_DEBUG 0
+#endif
+
+// Element extents a tile may address: gradient / parameter storage of p
+// (d0_p * inner_p), the fp32 shard of p (c_p * inner_p), and one rank-major
+// buffer or slot (N * S).
+struct Extents {
+  const int64_t* grad_numel = nullptr;   // [P]
+  const int64_t* shard_numel = nullptr;  // [P]
+  int64_t buf_numel = 0;
+  int32_t num_params = 0;
+  int32_t num_ranks = 0;
+};
+
+// What a tile list feeds: its source and destination extents and the element
+// alignment a 16-byte vector tile needs on each side.
+enum TileKind : int { kKindRs = 0, kKindStagedRs = 1, kKindCopy = 2, kKindPack = 3 };
+
+// True when `t` only addresses elements inside the extents of its kind:
+// parameter and rank in range, non-negative offsets and length,
+// src + len and dst + len within their buffers (the source of a zero tile
+// is not read), known flags, zero tiles only in reduce-scatter lists, and the
+// element alignment a vector tile's 16-byte accesses need.  Used by the
+// kernels of a debug build and by tide_layout_check_tiles on the host.
+__host__ __device__ inline bool tile_in_range(const Tile& t, int kind, const Extents& e) {
+  if (t.p < 0 || t.p >= e.num_params || t.r < 0 || t.r >= e.num_ranks) return false;
+  if (t.len < 0 || t.src < 0 || t.dst < 0) return false;
+  if (t.flags & ~(kTileZero | kTileVec)) return false;
+  const int64_t gn = e.grad_numel[t.p], sn = e.shard_numel[t.p], bn = e.buf_numel;
+  int64_t src_n = 0, dst_n = 0, src_al = 8, dst_al = 8;
+  switch (kind) {
+    case kKindRs: src_n = gn; dst_n = sn; dst_al = 4; break;
+    case kKindStagedRs: src_n = bn; dst_n = sn; dst_al = 4; break;
+    case kKindCopy: src_n = bn; dst_n = gn; break;  // placement; staging runs it backwards
+    case kKindPack: src_n = sn; dst_n = bn; src_al = 4; break;
+    default: return false;
+  }
+  const bool zero = (t.flags & kTileZero) != 0;
+  if (zero && kind != kKindRs && kind != kKindStagedRs) return false;
+  if (!zero && t.src > src_n - t.len) return false;
+  if (t.dst > dst_n - t.len) return false;
+  if (t.flags & kTileVec) {
+    if (!zero && t.src % src_al != 0) return false;
+    if (t.dst % dst_al != 0) return false;
+  }
+  return true;
+}
+
 // Launch and tiling constants.  Each can be overridden at build time with the
 // macro of the same name (used to sweep launch shapes).
 #ifndef TIDE_RS_THREADS
@@ -73,6 +124,8 @@ struct RsArgs {
   int* err = nullptr;
   uint64_t timeout_ns = 0;
   uint64_t test_stall_ns = 0;
+  Extents ext;  // checked per tile in debug builds (unchecked when ext.grad_numel is null)
+  int kind = kKindRs;
 };
 
 // All-gather input pack: stab[r * P + p] is rank r's fp32 shard of p (only
@@ -83,6 +136,8 @@ struct PackArgs {
   const float* const* stab;
   uint16_t* buf;
   int32_t num_params;
+  int* err = nullptr;
+  Extents ext;
 };
 
 struct AgArgs {
@@ -95,6 +150,7 @@ struct AgArgs {
   int* err;
   uint64_t timeout_ns;
   uint64_t test_stall_ns;
+  Extents ext;
 };
 
 #ifndef TIDE_BULK_STAGES
@@ -106,8 +162,9 @@ struct AgArgs {
 #ifndef TIDE_BULK_TIMEOUT_NS  // bound of every mbarrier wait of the bulk kernel
 #define TIDE_BULK_TIMEOUT_NS 2000000000ull
 #endif
-// Error codes written to the device error word.
-constexpr int kDevErrTimeout = 1;
+// Error bits OR-ed into the device error word.
+constexpr int kDevErrTimeout = 1;  // a bounded wait ran out
+constexpr int kDevErrRange = 2;    // debug builds: a tile failed tile_in_range and was skipped
 
 // Kernel launchers (kernels.cu).  Return the launch's cudaError_t.  `fat`
 // selects the kFatThreads-wide CTA used by the CTA-capped mode: a capped CTA
@@ -179,7 +236,8 @@ struct tide_layout_s {
   tide::Tile* d_pk_tiles = nullptr;
   tide::Tile* d_st_tiles = nullptr;  // RS tiles whose sources are slot offsets
   int num_sms = 0;
-  int* d_err = nullptr;         // device error word of the bulk-copy kernels
+  int* d_err = nullptr;         // device error word (bounded waits; range checks of debug builds)
+  int64_t* d_extents = nullptr;  // [2P]: d0_p*inner_p, then c_p*inner_p
   // The tile lists and error word are uploaded on the stream of the first
   // compute call, from pinned staging kept until destroy; calls on other
   // streams wait on tables_ev until it has been seen complete.

@@ -39,6 +39,9 @@ class Layout:
     def tiles(self, op: int):
         return _t.tide_layout_tiles(self.handle, op)
 
+    def check_tiles(self, op: int, rows) -> int:
+        return _t.tide_layout_check_tiles(self.handle, op, rows)
+
     def launch_shape(self, op: int):
         return _t.tide_layout_launch_shape(self.handle, op)
 

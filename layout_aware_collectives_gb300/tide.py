@@ -18,7 +18,9 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libtide.so")
+# TIDE_LIBRARY=debug loads the build whose kernels range-check every tile
+# (libtide_debug.so); anything else loads the release library.
+LIB_PATH = os.path.join(_HERE, "libtide_debug.so" if os.environ.get("TIDE_LIBRARY") == "debug" else "libtide.so")
 
 TIDE_OK = 0
 TIDE_ERR_INVALID_ARG = 1
@@ -27,6 +29,7 @@ TIDE_ERR_UNSUPPORTED = 3
 TIDE_ERR_CUDA = 4
 TIDE_ERR_TIMEOUT = 5
 TIDE_ERR_OUT_OF_MEMORY = 6
+TIDE_ERR_RANGE = 7
 
 TIDE_MODE_UNCAPPED = 0
 TIDE_MODE_CAPPED = 1
@@ -84,6 +87,8 @@ _sig("tide_rs_stage_bf16", _st, _vp, _vp, _vp, _vp)
 _sig("tide_rs_staged_bf16_to_fp32", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
 _sig("tide_layout_check_device", _st, _vp)
 _sig("tide_layout_set_test_stall", _st, _vp, ctypes.c_int64)
+_sig("tide_layout_check_tiles", _st, _vp, ctypes.c_int, _vp, ctypes.c_int64, _i64p)
+_sig("tide_build_info", ctypes.c_char_p)
 _sig("tide_status_string", ctypes.c_char_p, _st)
 _sig("tide_last_error", ctypes.c_char_p)
 
@@ -149,6 +154,20 @@ def tide_layout_check_device(layout) -> None:
 
 def tide_layout_set_test_stall(layout, ns: int) -> None:
     _check(_lib.tide_layout_set_test_stall(layout, ns), "tide_layout_set_test_stall")
+
+
+def tide_layout_check_tiles(layout, op: int, rows) -> int:
+    """Index of the first tile of `rows` ((n, 6) int64, as tide_layout_tiles
+    returns) that fails the kernels' range test, or -1."""
+    r = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 6)
+    bad = ctypes.c_int64(0)
+    _check(_lib.tide_layout_check_tiles(layout, op, r.ctypes.data if r.size else 0, r.shape[0],
+                                        ctypes.byref(bad)), "tide_layout_check_tiles")
+    return bad.value
+
+
+def tide_build_info() -> str:
+    return _lib.tide_build_info().decode()
 
 
 def tide_status_string(status: int) -> str:

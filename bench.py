@@ -56,6 +56,9 @@ def parse():
                     help="kernel mode of the timed step")
     ap.add_argument("--cap", type=int, default=0, help="CTA cap for --mode capped / bulk")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--collective", default="replicas", choices=["replicas", "ipc"],
+                    help="replicas: every process runs all N simulated ranks on its own GPU; "
+                         "ipc: one process per rank (N = world size), peers' buffers mapped over CUDA IPC")
     return ap.parse_args()
 
 
@@ -1080,10 +1083,127 @@ def interference_summary(res):
             "rows": rows}
 
 
+def run_ipc(args):
+    """One process per rank (N = world size) over peer memory: rank r keeps its
+    own gradients of every parameter and its rank-major buffer, maps its
+    peers' (CUDA IPC), and each step runs the single-rank reduce-scatter on
+    the pointer table of every rank's gradients, packs its shard into its own
+    block, waits on the host for every rank's pack, places every block
+    straight from its rank's buffer, and waits again.  Ranks map to devices
+    round-robin; handles, barriers and the max-over-ranks time go over gloo.
+    With fewer GPUs than ranks the processes share GPUs: a functional run of
+    the multi-process path, not a multi-GPU measurement."""
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    ndev = torch.cuda.device_count()
+    torch.cuda.set_device(local % ndev)
+    if world > 1:
+        dist.init_process_group("gloo")
+    import layout_aware_collectives_gb300 as tide
+    from layout_aware_collectives_gb300 import ipc
+    import synth
+    from synth.device import fill_bf16
+
+    base = synth.WORKLOADS[args.config]()
+    wl = synth.Workload(f"{base.name}_ipc{world}", world, base.shapes, base.names, base.sigma, base.seed,
+                        base.outlier_every, base.outlier_mult, base.zero_groups, base.zero_pct)
+    lay = tide.Layout(wl.shapes, world)
+    P = wl.num_params
+    numels = [synth.numel(s) for s in wl.shapes]
+    offs, total = ipc.arena_offsets(numels, 2)
+    arena = torch.empty(total // 2, dtype=torch.int16, device="cuda")
+    for p, (o, n) in enumerate(zip(offs, numels)):
+        if n and not wl.zero_grad(rank, p):
+            fill_bf16(arena[o // 2: o // 2 + n], wl.grad_key(rank, p), 0, wl.sigma, wl.outlier_every,
+                      wl.outlier_mult)
+        elif n:
+            arena[o // 2: o // 2 + n].zero_()
+    S = lay.block_numel
+    gathered = torch.zeros(world * S, dtype=torch.int16, device="cuda")
+    shards = [torch.empty(lay.shard_numel(p), dtype=torch.float32, device="cuda") for p in range(P)]
+    params = [torch.empty(n, dtype=torch.int16, device="cuda") for n in numels]
+    torch.cuda.synchronize()
+    mine = {"grads": tide.tide_ipc_export(arena), "gathered": tide.tide_ipc_export(gathered)}
+    ex = ipc.exchange(mine) if world > 1 else [mine]
+    peers = ipc.PeerMap()
+    gtab = tide.PointerTable(ipc.grad_table(ipc.rank_addresses(ex, rank, "grads", arena.data_ptr(), peers), offs))
+    btab = tide.PointerTable(ipc.rank_addresses(ex, rank, "gathered", gathered.data_ptr(), peers))
+    stab, ptab = tide.PointerTable(shards), tide.PointerTable(params)
+    stream = torch.cuda.Stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        lay.reduce_scatter_rank(rank, gtab, stab, wl.scale, stream)
+        if ev:
+            ev[1].record(stream)
+        lay.pack(rank, stab, gathered, stream)
+        stream.synchronize()
+        barrier(world)  # every rank's block is packed before anyone reads it
+        if ev:
+            ev[2].record(stream)
+        lay.place_ranks(btab, ptab, stream)
+        if ev:
+            ev[3].record(stream)
+        stream.synchronize()
+        barrier(world)  # every peer has read this rank's block before it is packed again
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = reduce_max((time.perf_counter() - t0) * 1e3 / K, world)
+    rs_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ag_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    # bytes every rank moves per step: its reduce-scatter (N bf16 reads and one
+    # fp32 write per valid element of its shards), its pack (6 bytes per
+    # padded shard element) and the placement of every parameter (4 bytes per
+    # element)
+    dims = [synth.dim0_inner(s) for s in wl.shapes]
+    total_bytes = 0
+    for r in range(world):
+        valid = sum(lay.valid_rows(p, r) * inner for p, (_, inner) in enumerate(dims))
+        padded = sum(lay.shard_numel(p) for p in range(P))
+        total_bytes += (2 * world + 4) * valid + 6 * padded + 4 * wl.psi
+    value = total_bytes / (step_ms * 1e-3) / 1e9
+    if rank == 0:
+        emit({"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": min(world, ndev),
+              "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(step_ms, 4),
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+              "data": "synthetic", "collective": "ipc",
+              "config": {"workload": wl.name, "num_ranks": world, "num_params": P, "psi": wl.psi,
+                         "parallelism": f"ipc ranks x{world} on {min(world, ndev)} GPU(s)",
+                         "step": "RS of this rank over every rank's gradients + pack + host barrier + "
+                                 "placement from every rank's buffer + host barrier"},
+              "rank0_kernels": {"rs_ms": round(rs_ms, 4), "place_ms": round(ag_ms, 4)},
+              "note": "ranks share GPUs when there are fewer GPUs than ranks: a functional run of the "
+                      "multi-process path, not a multi-GPU measurement"}, args)
+    barrier(world)
+    peers.close()
+    barrier(world)
+    lay.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.collective == "ipc":
+        return run_ipc(args)
     if args.hbm_mix_only:
         import torch
 

@@ -281,6 +281,25 @@ TIDE_API tide_status_t tide_rs_bf16_to_fp32_rank(tide_layout_t layout, int32_t r
                                                  float scale, cudaStream_t stream);
 
 /*
+ * Placement from per-rank buffers: TIDE-AG delivers each rank's shards
+ * straight into parameter storage ("TIDE的设计思路").  With one process per
+ * rank, rank r's packed block sits in rank r's own rank-major buffer; this
+ * call reads every rank's block from that rank's buffer, so no all-gather
+ * copy into a local buffer precedes the placement:
+ *   params[p][i*inner_p + j] = gathered[r][r*S + o_p + (i - r*c_p)*inner_p + j],  r = i / c_p.
+ * With gathered[k] all equal it is tide_ag_place.
+ *   gathered  host array of N device pointers, each to a whole N*S bf16
+ *             rank-major buffer (16-byte aligned; only block k of
+ *             gathered[k] is read), e.g. peers' buffers from tide_ipc_open;
+ *   params    host array of P device pointers, as for tide_ag_place.
+ * Runs the load/store placement kernel in every mode but
+ * TIDE_MODE_COPY_ENGINE (one cudaMemcpyAsync per parameter and rank).
+ * Bit copy.
+ */
+TIDE_API tide_status_t tide_ag_place_ranks(tide_layout_t layout, const uint16_t* const* gathered,
+                                           uint16_t* const* params, cudaStream_t stream);
+
+/*
  * All-gather input pack: FSDP2 gathers each rank's padded shard in the bf16
  * parameter dtype, so after the optimizer step a rank casts its fp32 shard
  * to bf16 into its slot of the rank-major buffer ("FSDP2通信开销的根源"):
@@ -373,6 +392,37 @@ TIDE_API tide_status_t tide_rs_staged_bf16_to_fp32(tide_layout_t layout, const u
 TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t layout, const uint16_t* const* grads,
                                                     float* const* shards, float scale,
                                                     cudaStream_t stream);
+
+/*
+ * Rank processes: peer memory.  With one process per rank, TIDE-RS reads
+ * every rank's per-parameter bf16 gradients directly
+ * ("FSDP通信终局：TIDE零拷贝集合通信优化" §TIDE的设计思路) and each rank keeps only
+ * its own shard; the data a rank brings in from its peers is (N-1)/N of the
+ * reduce-scatter input ("通信量分析" §带宽饱和和节点扩展).  These calls map a
+ * peer's buffers into this process so that rank r runs
+ * tide_rs_bf16_to_fp32_rank(r) with a pointer table whose entries for the
+ * other ranks are their gradients, and reads its peers' packed blocks of
+ * the rank-major buffer before tide_ag_place.  No multicast, no library
+ * collective: the loads are the library's own kernels (keep such calls in
+ * TIDE_MODE_UNCAPPED or TIDE_MODE_CAPPED: the TMA kernels of TIDE_MODE_BULK
+ * are for this process's own memory).  Tested with every rank process on
+ * one GPU; across GPUs the devices must have peer access.
+ *
+ *   tide_ipc_export: `handle` (TIDE_IPC_HANDLE_BYTES bytes) receives the IPC
+ *     handle of the cudaMalloc allocation that contains device pointer
+ *     `ptr`, `offset` the byte offset of `ptr` in it.  The allocation must
+ *     stay alive until every peer has closed it.
+ *   tide_ipc_open: maps the allocation of a peer's handle into this process
+ *     (on the current device); `base` receives its address, to which the
+ *     peer's offsets are added.  A handle is opened once per process.
+ *   tide_ipc_close: unmaps a base returned by tide_ipc_open.
+ * Errors: TIDE_ERR_INVALID_ARG (NULL, or a pointer outside any device
+ * allocation), TIDE_ERR_CUDA (the CUDA IPC call failed).
+ */
+#define TIDE_IPC_HANDLE_BYTES 64
+TIDE_API tide_status_t tide_ipc_export(const void* ptr, uint8_t* handle, uint64_t* offset);
+TIDE_API tide_status_t tide_ipc_open(const uint8_t* handle, void** base);
+TIDE_API tide_status_t tide_ipc_close(void* base);
 
 /*
  * Device-side failure report.  Synchronises the device, then reads and clears

@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(THREADS) ag_kernel(AgArgs a) {
       src = a.ptab[tile.p] + tile.dst;
       dst = const_cast<uint16_t*>(a.buf) + tile.src;
     } else {
-      src = a.buf + tile.src;
+      src = (a.bufs ? a.bufs[tile.r] : a.buf) + tile.src;
       dst = a.ptab[tile.p] + tile.dst;
     }
     if (tile.flags & kTileVec) {

@@ -593,6 +593,69 @@ tide_status_t tide_ag_place(tide_layout_t l, const uint16_t* gathered, uint16_t*
   return mark_used(l, slot, stream);
 }
 
+tide_status_t tide_ag_place_ranks(tide_layout_t l, const uint16_t* const* gathered, uint16_t* const* params,
+                                  cudaStream_t stream) {
+  if (!l) return set_error(TIDE_ERR_INVALID_ARG, "layout is NULL");
+  const int32_t N = l->num_ranks, P = l->num_params;
+  if (!gathered) return set_error(TIDE_ERR_INVALID_ARG, "gathered table is NULL");
+  if (P > 0 && !params) return set_error(TIDE_ERR_INVALID_ARG, "params table is NULL");
+  std::lock_guard<std::mutex> g(l->mu);
+  for (int32_t k = 0; k < N; ++k) {
+    tide_status_t st = check_ptr(gathered[k], l->block_numel * N, "gathered", k);
+    if (st != TIDE_OK) return st;
+  }
+  for (int32_t p = 0; p < P; ++p) {
+    tide_status_t st = check_ptr(params[p], l->d0[p] * l->inner[p], "params", p);
+    if (st != TIDE_OK) return st;
+  }
+  if (l->ag_tiles.empty()) return TIDE_OK;
+  tide_status_t st = ensure_device(l, stream);
+  if (st != TIDE_OK) return st;
+  if (l->mode == TIDE_MODE_COPY_ENGINE) {  // one copy per (parameter, rank) with rows
+    for (int32_t p = 0; p < P; ++p) {
+      const int64_t c = l->chunk[p], inner = l->inner[p];
+      for (int32_t r = 0; r < N; ++r) {
+        const int64_t v = std::max<int64_t>(0, std::min<int64_t>(c, l->d0[p] - (int64_t)r * c)) * inner;
+        if (v == 0) continue;
+        TIDE_CUDA(cudaMemcpyAsync(params[p] + (int64_t)r * c * inner,
+                                  gathered[r] + (int64_t)r * l->block_numel + l->offset[p], (size_t)v * 2,
+                                  cudaMemcpyDeviceToDevice, stream),
+                  "cudaMemcpyAsync");
+      }
+    }
+    return TIDE_OK;
+  }
+  // device table: P parameter pointers, then the N rank buffers
+  const TableKey key = make_key(TIDE_OP_AG, -2, (const void* const*)params, (size_t)P,
+                                (const void* const*)gathered, (size_t)N);
+  PtrSlot* slot = nullptr;
+  st = acquire_table(
+      l, key, (size_t)P + (size_t)N,
+      [&](void** dst) {
+        std::memcpy(dst, params, (size_t)P * sizeof(void*));
+        std::memcpy(dst + P, gathered, (size_t)N * sizeof(void*));
+      },
+      stream, &slot);
+  if (st != TIDE_OK) return st;
+  AgArgs a;
+  a.tiles = l->d_ag_tiles;
+  a.num_tiles = (int64_t)l->ag_tiles.size();
+  a.buf = gathered[0];
+  a.ptab = (uint16_t* const*)slot->d_table;
+  a.bufs = (const uint16_t* const*)(slot->d_table + P);
+  a.err = l->d_err;
+  a.timeout_ns = TIDE_BULK_TIMEOUT_NS;
+  a.test_stall_ns = 0;
+  a.ext = extents_of(l);
+  // the load/store kernel in every mode (the TMA copies are for this
+  // process's own memory): `cap` CTAs when capped, else one per tile
+  const bool capped = l->mode == TIDE_MODE_CAPPED;
+  const int grid = grid_for(a.num_tiles, capped ? TIDE_MODE_CAPPED : TIDE_MODE_UNCAPPED, l->cta_cap, l->num_sms, 0);
+  cudaError_t e = launch_ag(a, grid, capped, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "placement kernel launch");
+  return mark_used(l, slot, stream);
+}
+
 tide_status_t tide_ag_pack_bf16(tide_layout_t l, int32_t rank, const float* const* shards,
                                 uint16_t* gathered, cudaStream_t stream) {
   if (!l) return set_error(TIDE_ERR_INVALID_ARG, "layout is NULL");

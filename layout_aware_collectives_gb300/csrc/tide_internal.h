@@ -145,6 +145,10 @@ struct AgArgs {
   int64_t num_tiles;
   const uint16_t* buf;
   uint16_t* const* ptab;
+  // placement only: when set, rank r's block is read from bufs[r] (each a
+  // whole N*S rank-major buffer, e.g. rank r's own buffer mapped from its
+  // process) instead of from buf
+  const uint16_t* const* bufs = nullptr;
   // bulk-copy kernel only: error word set when a bounded wait runs out,
   // the bound, and a test hook that makes the first wait run out
   int* err;

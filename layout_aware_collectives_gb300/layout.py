@@ -79,6 +79,9 @@ class Layout:
     def place(self, gathered, params, stream=None) -> None:
         _t.tide_ag_place(self.handle, gathered, params, stream)
 
+    def place_ranks(self, gathered, params, stream=None) -> None:
+        _t.tide_ag_place_ranks(self.handle, gathered, params, stream)
+
     # -------- lifetime
     def close(self) -> None:
         if getattr(self, "handle", None):

@@ -43,6 +43,7 @@ TIDE_OP_STAGE = 3
 TIDE_OP_STAGED_RS = 4
 
 TIDE_MAX_RANKS = 4096
+TIDE_IPC_HANDLE_BYTES = 64
 TIDE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -82,11 +83,15 @@ _sig("tide_rs_bf16_to_fp32", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
 _sig("tide_ag_place", _st, _vp, _vp, _vp, _vp)
 _sig("tide_rs_bf16_to_fp32_noalloc", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
 _sig("tide_rs_bf16_to_fp32_rank", _st, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_float, _vp)
+_sig("tide_ag_place_ranks", _st, _vp, _vp, _vp, _vp)
 _sig("tide_ag_pack_bf16", _st, _vp, ctypes.c_int32, _vp, _vp, _vp)
 _sig("tide_rs_stage_bf16", _st, _vp, _vp, _vp, _vp)
 _sig("tide_rs_staged_bf16_to_fp32", _st, _vp, _vp, _vp, ctypes.c_float, _vp)
 _sig("tide_layout_check_device", _st, _vp)
 _sig("tide_layout_set_test_stall", _st, _vp, ctypes.c_int64)
+_sig("tide_ipc_export", _st, _vp, _vp, ctypes.POINTER(ctypes.c_uint64))
+_sig("tide_ipc_open", _st, _vp, ctypes.POINTER(_vp))
+_sig("tide_ipc_close", _st, _vp)
 _sig("tide_layout_check_tiles", _st, _vp, ctypes.c_int, _vp, ctypes.c_int64, _i64p)
 _sig("tide_build_info", ctypes.c_char_p)
 _sig("tide_status_string", ctypes.c_char_p, _st)
@@ -164,6 +169,28 @@ def tide_layout_check_tiles(layout, op: int, rows) -> int:
     _check(_lib.tide_layout_check_tiles(layout, op, r.ctypes.data if r.size else 0, r.shape[0],
                                         ctypes.byref(bad)), "tide_layout_check_tiles")
     return bad.value
+
+
+def tide_ipc_export(ptr) -> tuple[bytes, int]:
+    """(IPC handle of the allocation holding ptr, byte offset of ptr in it)."""
+    h = (ctypes.c_uint8 * TIDE_IPC_HANDLE_BYTES)()
+    off = ctypes.c_uint64(0)
+    _check(_lib.tide_ipc_export(_addr(ptr), h, ctypes.byref(off)), "tide_ipc_export")
+    return bytes(h), off.value
+
+
+def tide_ipc_open(handle: bytes) -> int:
+    """Base address of a peer's exported allocation mapped into this process."""
+    if len(handle) != TIDE_IPC_HANDLE_BYTES:
+        raise ValueError("an IPC handle is 64 bytes")
+    h = (ctypes.c_uint8 * TIDE_IPC_HANDLE_BYTES).from_buffer_copy(handle)
+    base = ctypes.c_void_p(0)
+    _check(_lib.tide_ipc_open(h, ctypes.byref(base)), "tide_ipc_open")
+    return base.value
+
+
+def tide_ipc_close(base: int) -> None:
+    _check(_lib.tide_ipc_close(base), "tide_ipc_close")
 
 
 def tide_build_info() -> str:
@@ -318,6 +345,12 @@ def tide_ag_place(layout, gathered, params, stream=None) -> None:
     """gathered: N*S bf16 rank-major buffer; params: P bf16 parameter pointers."""
     t = _table(params)
     _check(_lib.tide_ag_place(layout, _addr(gathered), _tptr(t), _stream(stream)), "tide_ag_place")
+
+
+def tide_ag_place_ranks(layout, gathered, params, stream=None) -> None:
+    """gathered: N rank-major bf16 buffers (block k read from buffer k); params: P pointers."""
+    g, t = _table(gathered), _table(params)
+    _check(_lib.tide_ag_place_ranks(layout, _tptr(g), _tptr(t), _stream(stream)), "tide_ag_place_ranks")
 
 
 def exported_symbols():

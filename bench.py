@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stock", action="store_true")
     ap.add_argument("--no-hbm-mix", action="store_true")
+    ap.add_argument("--no-next-ops", action="store_true",
+                    help="skip the single-rank RS, pack and Slot-Reuse figures")
     ap.add_argument("--hbm-mix-only", action="store_true",
                     help="only measure the HBM read/write-mix streams and print them as one JSON line")
     ap.add_argument("--no-second", action="store_true",
@@ -475,7 +477,8 @@ def run_tide(args):
 
     layout.check_device()  # raises if a bounded device wait ran out during the timed steps
     layout.set_mode(tide.TIDE_MODE_UNCAPPED)
-    out["next_ops"] = run_next_ops(tide, layout, job, wl, stream)
+    if not args.no_next_ops:
+        out["next_ops"] = run_next_ops(tide, layout, job, wl, stream)
     if not args.no_stock:
         out["stock_fsdp2"] = run_stock(job, wl, stream, rs_avg, ag_avg)
     if not args.no_e2e:

@@ -456,9 +456,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(bar)) : "memory");
 }
 
-// Elements per rank slice for a stage of about `stage` bytes (a multiple of
-// 8, so every slice is a multiple of 16 bytes).
-__device__ __host__ __forceinline__ int rs_chunk_elems(int n, int stage) { return (stage / 2 / n) & ~7; }
 
 }  // namespace bulk
 
@@ -478,13 +475,40 @@ __device__ __forceinline__ void rs_scalar_run(const RsArgs& a, const Tile& tile,
   }
 }
 
+// Ring geometry of the TMA-staged reduce-scatter, shared by the launcher and
+// the kernel.  A stage holds the slices of G ranks (G = N: one stage per
+// chunk; G < N: rank-group staging, a chunk spans `groups` consecutive
+// stages), each slice E elements (a multiple of 8, so every copy is a
+// multiple of 16 bytes).
+struct RsBulkGeom {
+  int G, groups, E;
+  uint32_t slice, stage;
+  int S;
+};
+
+__device__ __host__ __forceinline__ RsBulkGeom rs_bulk_geom(int n, int stage_target, int rank_group) {
+  RsBulkGeom g;
+  g.G = (rank_group > 0 && rank_group < n) ? rank_group : n;
+  g.groups = (n + g.G - 1) / g.G;
+  g.E = (stage_target / 2 / g.G) & ~7;
+  g.slice = (uint32_t)g.E * 2u;
+  g.stage = g.slice * (uint32_t)g.G;
+  const size_t fit = g.stage ? kRsBulkRing / g.stage : 0;
+  g.S = (int)(fit < (size_t)kRsBulkMaxStages ? fit : (size_t)kRsBulkMaxStages);
+  return g;
+}
+
+// Rank-group staging keeps every consumer thread's partial sums of a chunk
+// in registers across the chunk's stages: at most this many 8-element
+// vectors per thread (a slice of up to 8 KiB).
+constexpr int kRsBulkGroupVecs = 2;
+
 __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
   extern __shared__ __align__(128) unsigned char rs_smem[];
   const int N = a.num_ranks;
-  const int E = bulk::rs_chunk_elems(N, a.stage_bytes);
-  const uint32_t slice = (uint32_t)E * 2;          // bytes per rank per chunk
-  const uint32_t stage_bytes = slice * (uint32_t)N;
-  const int S = min(kRsBulkMaxStages, (int)(kRsBulkRing / stage_bytes));
+  const RsBulkGeom geo = rs_bulk_geom(N, a.stage_bytes, a.rank_group);
+  const int E = geo.E, S = geo.S, G = geo.G, groups = geo.groups;
+  const uint32_t slice = geo.slice, stage_bytes = geo.stage;
   uint64_t* full = (uint64_t*)(rs_smem + (size_t)S * stage_bytes);
   uint64_t* empty = full + S;
   const uint16_t** ptrs = (const uint16_t**)(empty + S);  // producer's current sources
@@ -506,7 +530,7 @@ __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
 
   if (warp == 0) {  // ---------------- producer
     const uint64_t pol = evict_first_policy_rs();
-    int64_t j = 0;
+    int64_t j = 0;  // stages issued
     for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
       const Tile tile = a.tiles[t];
       if (!tile_ok(tile, a.kind, a.ext, a.err, false)) continue;  // the consumers report it
@@ -516,25 +540,28 @@ __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
       __syncwarp();
       for (int k = lane; k < N; k += 32) ptrs[k] = a.gtab[(int64_t)tile.p * N + k] + tile.src;
       __syncwarp();
-      for (int off = 0; off < vec; off += E, ++j) {
+      for (int off = 0; off < vec; off += E) {
         const int n = min(E, vec - off);
-        const int s = (int)(j % S);
-        if (j >= S) {  // the consumers released this stage's previous chunk
-          int ok = lane == 0 ? (int)bulk::mbar_wait(&empty[s], (uint32_t)(((j / S) + 1) & 1), a.timeout_ns) : 0;
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) {
-            if (lane == 0) atomicOr(a.err, kDevErrTimeout);
-            // loads issued into the ring may still land: wait (bounded) for them
-            for (int64_t k = (j >= S ? j - S : 0); k < j; ++k)
-              if (lane == 0) bulk::mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), a.timeout_ns);
-            return;
+        for (int g = 0; g < groups; ++g, ++j) {  // the chunk's rank groups, in rank order
+          const int k0 = g * G, gk = min(G, N - k0);
+          const int s = (int)(j % S);
+          if (j >= S) {  // the consumers released this stage's previous contents
+            int ok = lane == 0 ? (int)bulk::mbar_wait(&empty[s], (uint32_t)(((j / S) + 1) & 1), a.timeout_ns) : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+              if (lane == 0) atomicOr(a.err, kDevErrTimeout);
+              // loads issued into the ring may still land: wait (bounded) for them
+              for (int64_t k = (j >= S ? j - S : 0); k < j; ++k)
+                if (lane == 0) bulk::mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), a.timeout_ns);
+              return;
+            }
           }
+          if (lane == 0) bulk::mbar_expect_tx(&full[s], (uint32_t)gk * (uint32_t)n * 2u);
+          __syncwarp();
+          unsigned char* st = rs_smem + (size_t)s * stage_bytes;
+          for (int k = lane; k < gk; k += 32)
+            bulk::g2s(st + (size_t)k * slice, ptrs[k0 + k] + off, (uint32_t)n * 2u, &full[s], pol);
         }
-        if (lane == 0) bulk::mbar_expect_tx(&full[s], (uint32_t)N * (uint32_t)n * 2u);
-        __syncwarp();
-        unsigned char* st = rs_smem + (size_t)s * stage_bytes;
-        for (int k = lane; k < N; k += 32)
-          bulk::g2s(st + (size_t)k * slice, ptrs[k] + off, (uint32_t)n * 2u, &full[s], pol);
       }
     }
     return;
@@ -542,7 +569,7 @@ __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
 
   // ---------------- consumers
   const int cid = threadIdx.x - 32;
-  int64_t j = 0;
+  int64_t j = 0;  // stages consumed
   for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
     const Tile tile = a.tiles[t];
     if (!tile_ok(tile, a.kind, a.ext, a.err, cid == 0)) continue;  // the producer skips it too
@@ -556,27 +583,66 @@ __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
       continue;
     }
     const int vec = tile.len & ~7;
-    for (int off = 0; off < vec; off += E, ++j) {
-      const int n = min(E, vec - off);
-      const int s = (int)(j % S);
-      if (!bulk::mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.timeout_ns)) {
-        atomicOr(a.err, kDevErrTimeout);
-        return;
-      }
-      const unsigned char* st = rs_smem + (size_t)s * stage_bytes;
-      for (int v = cid; v < (n >> 3); v += kRsBulkConsumers) {
-        float acc[8];
+    for (int off = 0; off < vec; off += E) {
+      const int nv = min(E, vec - off) >> 3;
+      if (groups == 1) {  // one stage holds every rank's slice of the chunk
+        const int s = (int)(j % S);
+        if (!bulk::mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.timeout_ns)) {
+          atomicOr(a.err, kDevErrTimeout);
+          return;
+        }
+        const unsigned char* st = rs_smem + (size_t)s * stage_bytes;
+        for (int v = cid; v < nv; v += kRsBulkConsumers) {
+          float acc[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        for (int k = 0; k < N; ++k) add8(acc, *(const uint4*)(st + (size_t)k * slice + 16 * v));
-        float* o = out + off + 8 * v;
-        st_stream(o, __fmul_rn(acc[0], a.scale), __fmul_rn(acc[1], a.scale), __fmul_rn(acc[2], a.scale),
-                  __fmul_rn(acc[3], a.scale));
-        st_stream(o + 4, __fmul_rn(acc[4], a.scale), __fmul_rn(acc[5], a.scale), __fmul_rn(acc[6], a.scale),
-                  __fmul_rn(acc[7], a.scale));
+          for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+          for (int k = 0; k < N; ++k) add8(acc, *(const uint4*)(st + (size_t)k * slice + 16 * v));
+          float* o = out + off + 8 * v;
+          st_stream(o, __fmul_rn(acc[0], a.scale), __fmul_rn(acc[1], a.scale), __fmul_rn(acc[2], a.scale),
+                    __fmul_rn(acc[3], a.scale));
+          st_stream(o + 4, __fmul_rn(acc[4], a.scale), __fmul_rn(acc[5], a.scale), __fmul_rn(acc[6], a.scale),
+                    __fmul_rn(acc[7], a.scale));
+        }
+        __syncwarp();
+        if (lane == 0) bulk::mbar_arrive(&empty[s]);
+        ++j;
+        continue;
       }
-      __syncwarp();
-      if (lane == 0) bulk::mbar_arrive(&empty[s]);
+      // rank-group staging: the chunk's groups arrive in consecutive stages;
+      // each thread's vectors keep their sums in registers across them
+      float acc[kRsBulkGroupVecs][8];
+#pragma unroll
+      for (int u = 0; u < kRsBulkGroupVecs; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+      for (int g = 0; g < groups; ++g, ++j) {
+        const int s = (int)(j % S);
+        if (!bulk::mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.timeout_ns)) {
+          atomicOr(a.err, kDevErrTimeout);
+          return;
+        }
+        const int gk = min(G, N - g * G);
+        const unsigned char* st = rs_smem + (size_t)s * stage_bytes;
+#pragma unroll
+        for (int u = 0; u < kRsBulkGroupVecs; ++u) {
+          const int v = cid + u * kRsBulkConsumers;
+          if (v < nv)
+            for (int k = 0; k < gk; ++k) add8(acc[u], *(const uint4*)(st + (size_t)k * slice + 16 * v));
+        }
+        __syncwarp();
+        if (lane == 0) bulk::mbar_arrive(&empty[s]);
+      }
+#pragma unroll
+      for (int u = 0; u < kRsBulkGroupVecs; ++u) {
+        const int v = cid + u * kRsBulkConsumers;
+        if (v < nv) {
+          float* o = out + off + 8 * v;
+          st_stream(o, __fmul_rn(acc[u][0], a.scale), __fmul_rn(acc[u][1], a.scale),
+                    __fmul_rn(acc[u][2], a.scale), __fmul_rn(acc[u][3], a.scale));
+          st_stream(o + 4, __fmul_rn(acc[u][4], a.scale), __fmul_rn(acc[u][5], a.scale),
+                    __fmul_rn(acc[u][6], a.scale), __fmul_rn(acc[u][7], a.scale));
+        }
+      }
     }
     rs_scalar_run(a, tile, out, vec, cid, kRsBulkConsumers);  // < 8 element tail
   }
@@ -727,11 +793,10 @@ cudaError_t launch_ag_bulk(const AgArgs& a, int grid, bool to_buf, cudaStream_t 
 cudaError_t launch_rs_bulk(const RsArgs& a, int grid, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
   const int N = a.num_ranks;
-  if (bulk::rs_chunk_elems(N, a.stage_bytes) < 8) return cudaErrorInvalidValue;
-  const size_t stage_bytes = (size_t)bulk::rs_chunk_elems(N, a.stage_bytes) * 2 * N;
-  if (kRsBulkRing / stage_bytes < 2) return cudaErrorInvalidValue;
-  const int S = (int)std::min<size_t>(kRsBulkMaxStages, kRsBulkRing / stage_bytes);
-  const size_t smem = (size_t)S * stage_bytes + 16 * (size_t)S + 8 * (size_t)N;
+  const RsBulkGeom g = rs_bulk_geom(N, a.stage_bytes, a.rank_group);
+  if (g.E < 8 || g.S < 2) return cudaErrorInvalidValue;
+  if (g.groups > 1 && g.E > 8 * kRsBulkConsumers * kRsBulkGroupVecs) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)g.S * g.stage + 16 * (size_t)g.S + 8 * (size_t)N;
   cudaError_t e = cudaFuncSetAttribute(rs_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   rs_bulk_kernel<<<grid, kRsBulkThreads, smem, stream>>>(a);

@@ -119,8 +119,10 @@ struct RsArgs {
   int32_t num_params;
   float scale;
   // bulk-staged kernel only (see AgArgs); stage_bytes: target bytes of one
-  // ring stage (the N rank slices of a chunk)
+  // ring stage; rank_group: ranks per stage (0 or >= N: all N rank slices of
+  // a chunk in one stage; G < N: a chunk spans ceil(N / G) stages)
   int32_t stage_bytes = 0;
+  int32_t rank_group = 0;
   int* err = nullptr;
   uint64_t timeout_ns = 0;
   uint64_t test_stall_ns = 0;
@@ -162,6 +164,17 @@ struct AgArgs {
 #endif
 #ifndef TIDE_BULK_CHUNK  // bytes per bulk copy (multiple of 16)
 #define TIDE_BULK_CHUNK 16384
+#endif
+// TMA-staged reduce-scatter: bytes of one rank's slice of a chunk (over
+// every SM / capped), and the stage size of rank-group staging.
+#ifndef TIDE_RS_BULK_SLICE
+#define TIDE_RS_BULK_SLICE 4096
+#endif
+#ifndef TIDE_RS_BULK_SLICE_CAPPED
+#define TIDE_RS_BULK_SLICE_CAPPED 8192
+#endif
+#ifndef TIDE_RS_BULK_GROUP_STAGE
+#define TIDE_RS_BULK_GROUP_STAGE 65536
 #endif
 #ifndef TIDE_BULK_TIMEOUT_NS  // bound of every mbarrier wait of the bulk kernel
 #define TIDE_BULK_TIMEOUT_NS 2000000000ull

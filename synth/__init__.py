@@ -290,6 +290,9 @@ WORKLOADS = {
     "sweep16": lambda: sweep(16),
     "sweep32": lambda: sweep(32),
     "sweep64": lambda: sweep(64),
+    # the N = 64 sweep's recipe with [d0, 1024] parameters and 448 rows per
+    # rank: 3.8 GB of gradients, a profiler-sized case of the same kernels
+    "sweep64_small": lambda: sweep(64, inner=1024, rows_per_rank=448),
 }
 
 

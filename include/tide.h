@@ -134,10 +134,14 @@ typedef enum {
    * see tide_layout_check_device).  Placement and staging: global -> shared
    * -> global copies issued by one lane per CTA.  Reduce-scatter (all three
    * forms, N <= 512; larger N runs the load/store kernel): one 288-thread
-   * CTA per SM whose producer warp stages the N rank slices of each chunk
-   * (4 KiB per slice, 8 KiB when capped; 32 KiB to 96 KiB per chunk, 64 KiB
-   * to 96 KiB when capped) in a 192 KiB shared-memory ring
-   * and whose 8 consumer warps sum them.  The pack runs as in
+   * CTA per SM whose producer warp stages the rank slices of each chunk in a
+   * 192 KiB shared-memory ring of 64 KiB stages and whose 8 consumer warps
+   * sum them in ascending rank order.  Up to 16 ranks (8 when capped) one
+   * stage holds all N slices of a chunk (64 KiB / N each); above, a stage
+   * holds 16 ranks' 4 KiB slices (8 ranks' 8 KiB when capped) and a chunk
+   * spans consecutive stages, its partial sums kept in registers.  The
+   * no-allocation reduce-scatter and the per-rank placement run the
+   * load/store kernels in this mode.  The pack runs as in
    * TIDE_MODE_UNCAPPED.  cta_cap > 0 caps the grid at cta_cap CTAs (one per
    * SM), cta_cap = 0 uses every SM. */
   TIDE_MODE_BULK = 3

@@ -418,11 +418,13 @@ tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, cons
   a.test_stall_ns = (uint64_t)l->test_stall_ns;
   a.ext = extents_of(l);
   a.kind = staged ? kKindStagedRs : kKindRs;
-  // TMA-staged kernel.  Measured on GB300, rank slices of 4 KiB over every
+  // TMA-staged kernel.  Measured on GB300: rank slices of 4 KiB over every
   // SM (8 KiB when capped) keep the bulk-copy engine busy and smaller ones
-  // do not.  When all N slices of a chunk fit a stage of
-  // TIDE_RS_BULK_GROUP_STAGE bytes, a stage holds them (at least 32 KiB, 64
-  // KiB capped); above that N a stage holds the slices of
+  // do not, and 64 KiB stages (a 3-deep ring) beat 32 KiB ones (by 1-2% at
+  // N = 8, 12% with rank groups) and 96 KiB ones.  When all N slices of a
+  // chunk fit a stage of TIDE_RS_BULK_GROUP_STAGE bytes, one stage holds
+  // them (at least TIDE_RS_BULK_MIN_STAGE bytes, so slices grow as N
+  // shrinks); above that N a stage holds the slices of
   // TIDE_RS_BULK_GROUP_STAGE / slice ranks and a chunk spans consecutive
   // stages, so slices and ring depth no longer shrink as N grows.
   const int64_t slice_target = l->cta_cap > 0 ? TIDE_RS_BULK_SLICE_CAPPED : TIDE_RS_BULK_SLICE;
@@ -433,7 +435,8 @@ tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, cons
   } else {
     a.rank_group = 0;
     a.stage_bytes = (int32_t)std::min<int64_t>(
-        98304, std::max<int64_t>(l->cta_cap > 0 ? 65536 : 32768, (int64_t)l->num_ranks * slice_target));
+        98304, std::max<int64_t>(TIDE_RS_BULK_MIN_STAGE,
+                                 (int64_t)l->num_ranks * slice_target));
   }
   cudaError_t e = rs_uses_bulk(l) ? launch_rs_bulk(a, grid_of(l, t1 - t0, 1), stream)
                                   : launch_rs(a, grid_of(l, t1 - t0, 0), l->mode == TIDE_MODE_CAPPED,

@@ -176,6 +176,9 @@ struct AgArgs {
 #ifndef TIDE_RS_BULK_GROUP_STAGE
 #define TIDE_RS_BULK_GROUP_STAGE 65536
 #endif
+#ifndef TIDE_RS_BULK_MIN_STAGE  // smallest stage when a chunk's N slices fit one (over every SM)
+#define TIDE_RS_BULK_MIN_STAGE 65536
+#endif
 #ifndef TIDE_BULK_TIMEOUT_NS  // bound of every mbarrier wait of the bulk kernel
 #define TIDE_BULK_TIMEOUT_NS 2000000000ull
 #endif

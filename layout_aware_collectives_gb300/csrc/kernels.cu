@@ -649,9 +649,12 @@ __global__ void __launch_bounds__(kRsBulkThreads, 1) rs_bulk_kernel(RsArgs a) {
 }
 
 // ---------------------------------------------------------------- all-gather input pack
-// fp32 -> bf16 bits, round to nearest with ties to even on the 16 dropped
-// bits (the usual add-half-ulp-plus-lowest-kept-bit method); a NaN keeps its
-// sign and top payload and is made quiet.
+// fp32 -> bf16 bits, IEEE 754-2008 roundTiesToEven (§4.3.1) applied to the
+// 16 dropped bits.  Adding 0x7FFF plus the lowest kept bit carries into the
+// kept bits exactly when the dropped part is above half a bf16 ulp, or equal
+// to it with an odd kept part; a carry out of the mantissa steps the
+// exponent, which rounds the largest finite values up to infinity as the
+// rule requires.  A NaN keeps its sign and top payload and is made quiet.
 __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
   uint32_t u = __float_as_uint(f);
   if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (u >> 16) | 0x0040u;

@@ -129,8 +129,10 @@ int oracle_rs_rank(int32_t num_ranks, int32_t num_params, const int64_t* d0, con
   return 0;
 }
 
-/* Round to nearest even on the 16 bits dropped: add half an ulp of bf16
- * (0x7FFF) plus the lowest kept bit, then truncate. */
+/* IEEE 754-2008 roundTiesToEven (§4.3.1) on the 16 bits dropped: adding
+ * just under half a bf16 ulp (0x7FFF) plus the lowest kept bit carries into
+ * the kept bits exactly when the dropped part exceeds half an ulp, or equals
+ * it with an odd kept part; then truncate. */
 uint16_t oracle_f32_to_bf16(float f) {
   uint32_t u;
   memcpy(&u, &f, sizeof u);

@@ -75,7 +75,9 @@ SYNTH_FN float synth_mul(float a, float b) {
 #endif
 }
 
-/* bf16 bits of a finite fp32 value, round to nearest, ties to even. */
+/* bf16 bits of a finite fp32 value, IEEE 754-2008 roundTiesToEven on the
+ * 16 dropped bits (adding 0x7FFF plus the lowest kept bit carries exactly
+ * when the dropped part is above half an ulp, or equal with an odd kept part). */
 SYNTH_FN uint16_t synth_bf16_rne(float f) {
   uint32_t u = synth_f32_bits(f);
   u += 0x7FFFu + ((u >> 16) & 1u);

@@ -71,9 +71,10 @@
  *    tile, so the block scheduler dispatches the compute kernel's pending
  *    CTAs first and the collective fills what it leaves.  Measured on GB300
  *    beside a loop of bf16 8192^3 GEMMs over 0.3 s windows (power-capped
- *    clock): equal priority +284% GEMM time; low priority +9.6% with the
- *    reduce-scatter moving 0.33 TB/s, about what 8 capped CTAs cost (+8.8%,
- *    0.38 TB/s); capped 16 / 32 / 64 CTAs +13% / +24% / +52%.
+ *    clock; two runs): equal priority +279% to +284% GEMM time; low
+ *    priority +9.0% to +9.6% with the reduce-scatter moving 0.28-0.33 TB/s,
+ *    about what 8 capped CTAs cost (+8.8% to +9.0%, 0.37-0.38 TB/s); capped
+ *    16 / 32 / 64 CTAs +13-15% / +24-25% / +52-53%.
  *  - A layout may be used from several host threads (calls are serialised
  *    internally).  Calls on different streams that write the same output
  *    buffers race, as any two kernels would.

@@ -317,3 +317,32 @@ def test_small_layouts_spread_over_the_gpu():
     with tide.Layout([(8192, 8192)], 8) as lay:
         t = lay.tiles(tide.TIDE_OP_RS)
         assert t[:, 4].max() == 16384  # 256 KiB of bf16 reads over 8 ranks
+
+
+def test_place_ranks_and_ipc_validate_on_the_host():
+    """The per-rank placement checks its N buffer pointers and P parameter
+    pointers before anything touches a device; the IPC calls refuse NULL
+    arguments and malformed handles."""
+    shapes = [(8, 2), (5,)]
+    good = 0x10000
+    with tide.Layout(shapes, 2) as lay:
+        params = [good + 0x1000, good + 0x2000]
+        for bufs, status in (([good, None], tide.TIDE_ERR_INVALID_ARG),
+                             ([good, good + 8], tide.TIDE_ERR_MISALIGNED)):
+            with pytest.raises(tide.TideError) as e:
+                lay.place_ranks(bufs, params)
+            assert e.value.status == status
+        with pytest.raises(tide.TideError) as e:
+            lay.place_ranks([good, good], [good + 2, good])
+        assert e.value.status == tide.TIDE_ERR_MISALIGNED
+        with pytest.raises(tide.TideError) as e:
+            tide.tide_ag_place_ranks(lay.handle, None, params)
+        assert e.value.status == tide.TIDE_ERR_INVALID_ARG
+    from layout_aware_collectives_gb300 import tide as T
+
+    for call in (lambda: T._lib.tide_ipc_export(None, None, None),
+                 lambda: T._lib.tide_ipc_open(None, None),
+                 lambda: T._lib.tide_ipc_close(None)):
+        assert call() == tide.TIDE_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        tide.tide_ipc_open(b"short")

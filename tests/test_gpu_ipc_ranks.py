@@ -169,3 +169,35 @@ def test_ipc_export_refuses_memory_outside_device_allocations():
     assert h == h0 and off - off0 == 4096 and len(h) == tide.TIDE_IPC_HANDLE_BYTES
     torch.zeros(1, device="cuda").add_(1)  # no CUDA error left behind
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("mode", [(tide.TIDE_MODE_UNCAPPED, 0), (tide.TIDE_MODE_CAPPED, 3),
+                                  (tide.TIDE_MODE_BULK, 2), (tide.TIDE_MODE_COPY_ENGINE, 0)],
+                         ids=["uncapped", "capped3", "bulk_cap2", "copy_engine"])
+def test_place_ranks_reads_each_block_from_its_own_buffer(mode):
+    """N distinct buffers, buffer k holding real data only in block k and the
+    padding sentinel everywhere else: every rank's rows must come from that
+    rank's own buffer (a block read from another buffer brings sentinels
+    into the parameters), bit for bit the oracle's placement."""
+    from synth import SENTINEL_BF16
+
+    cases = [(synth.tiny(), 8),
+             (synth.custom("ragged_ranks5", 5, [(13, 24), (4, 7), (16,), (), (0, 8), (10, 3, 5)],
+                           sigma=0.5, seed=5), 1),
+             (synth.custom("ragged_ranks13", 13, [(40, 9), (12, 16), (3 * 13 + 1,), (26, 3, 5)],
+                           sigma=0.5, seed=13), 8)]
+    for wl, align in cases:
+        with tide.Layout(wl.shapes, wl.num_ranks, align_elems=align) as lay:
+            lay.set_mode(*mode)
+            job = DeviceJob(wl, lay, align=align)
+            S, N = lay.block_numel, job.N
+            bufs = []
+            for k in range(N):
+                b = torch.full_like(job.gathered, SENTINEL_BF16)
+                b[k * S:(k + 1) * S] = job.gathered[k * S:(k + 1) * S]
+                bufs.append(b)
+            torch.cuda.synchronize()
+            lay.place_ranks(bufs, job.param_ptrs())
+            torch.cuda.synchronize()
+            gpu_checks.full_check_ag(job)
+            assert job.guards_intact()

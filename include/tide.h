@@ -381,7 +381,8 @@ TIDE_API tide_status_t tide_rs_staged_bf16_to_fp32(tide_layout_t layout, const u
  * streams, or from different layouts without stream ordering between them)
  * race.  The first call on each device, and the first after the device's
  * CUDA context was replaced (cudaDeviceReset), looks up the array's device
- * address (cudaGetSymbolAddress) and copies the tables again.  The tables
+ * address (cudaGetSymbolAddress) and copies the tables again (every call
+ * does, if the driver cannot report a context id).  The tables
  * are copied from pageable host memory, so a call that copies returns only
  * once the stream's earlier work has completed and the driver has taken
  * its copy of them; calls on one device are serialised with each other

@@ -64,12 +64,15 @@
  *    such graphs are no longer replayed.
  *  - A failed CUDA call is reported through the status and cleared from the
  *    runtime's per-thread last error.
- *  - Next to compute kernels, either cap the CTAs (TIDE_MODE_CAPPED) or
- *    enqueue the calls on a low-priority stream
- *    (cudaStreamCreateWithPriority) and the compute on a higher-priority
- *    one: outside the capped mode every launch is one short-lived CTA per
- *    tile, so the block scheduler dispatches the compute kernel's pending
- *    CTAs first and the collective fills what it leaves.  Measured on GB300
+ *  - Next to compute kernels, either cap the CTAs (TIDE_MODE_CAPPED) or put
+ *    the compute on a stream of higher priority than the collective's
+ *    (cudaStreamCreateWithPriority): outside the capped mode every launch is
+ *    one short-lived CTA per tile, so the block scheduler dispatches the
+ *    compute kernel's pending CTAs first and the collective fills what it
+ *    leaves.  A stream's default priority is already the lowest (the range
+ *    is 0, the default, to -3 on GB300), so the collective needs no special
+ *    stream; the compute's stream must be raised, which only the caller can
+ *    do.  Measured on GB300
  *    beside a loop of bf16 8192^3 GEMMs over 0.3 s windows (power-capped
  *    clock; two runs): equal priority +279% to +284% GEMM time; low
  *    priority +9.0% to +9.6% with the reduce-scatter moving 0.28-0.33 TB/s,

@@ -945,19 +945,28 @@ def run_interference(tide, layout, job, wl, props, smi_dev, repeats=3, window_s=
         return e0.elapsed_time(e1) / count
 
     def concurrent(sg, sr, op, count, launches, nbytes):
-        """`launches` op launches on sr (an event pair each), then `count`
-        GEMMs on sg once the op loop runs: GEMM ms, bytes the op moved inside
-        the GEMM window, mean op launch ms."""
+        """`launches` op launches on sr (an event pair each), enqueued by a
+        second host thread, and `count` GEMMs on sg enqueued by this one once
+        the op loop has started: GEMM ms, bytes the op moved inside the GEMM
+        window, mean op launch ms.  Enqueuing both at once keeps an op whose
+        calls cost more host time than device time (the copy-engine
+        placement of many tensors) running beside the GEMMs."""
         evs = []
-        with torch.cuda.stream(sr):
-            for _ in range(launches):
-                x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                x0.record(sr)
-                op()
-                x1.record(sr)
-                evs.append((x0, x1))
+
+        def enqueue_ops():
+            with torch.cuda.stream(sr):
+                for _ in range(launches):
+                    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    x0.record(sr)
+                    op()
+                    x1.record(sr)
+                    evs.append((x0, x1))
+
+        th = threading.Thread(target=enqueue_ops)
+        th.start()
         time.sleep(0.002)
         e0, e1 = gemm_window(sg, count)
+        th.join()
         torch.cuda.synchronize()
         window = e0.elapsed_time(e1)
         moved = 0.0

@@ -76,8 +76,8 @@
  *    beside a loop of bf16 8192^3 GEMMs over 0.3 s windows (power-capped
  *    clock; 70B- and MoE-shaped layers): equal priority +279% to +593%
  *    GEMM time, depending on how the launches are submitted; low priority
- *    +8.6% to +9.6% with the reduce-scatter moving 0.28-0.33 TB/s, about
- *    what 8 capped CTAs cost (+8.8% to +9.2%, 0.37-0.39 TB/s); capped
+ *    +7.2% to +9.6% with the reduce-scatter moving 0.28-0.33 TB/s, about
+ *    what 8 capped CTAs cost (+7.4% to +9.2%, 0.37-0.39 TB/s); capped
  *    16 / 32 / 64 CTAs +13-15% / +23-25% / +50-53%.
  *  - A layout may be used from several host threads (calls are serialised
  *    internally).  Calls on different streams that write the same output

@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stock", action="store_true")
     ap.add_argument("--no-hbm-mix", action="store_true")
+    ap.add_argument("--no-sustained", action="store_true",
+                    help="skip the ~2 s back-to-back run with its clock record")
     ap.add_argument("--no-next-ops", action="store_true",
                     help="skip the single-rank RS, pack and Slot-Reuse figures")
     ap.add_argument("--hbm-mix-only", action="store_true",
@@ -402,6 +404,46 @@ def timed_steps(layout, job, wl, stream, K, warmup, world, smi_dev, l2_bytes):
             f"inputs larger than L2 ({(rs_bytes + ag_bytes) / 1e9:.1f} GB per step)"}
 
 
+def run_sustained(layout, job, wl, stream, smi_dev, world, seconds=2.0):
+    """The same step back to back for about `seconds` (after the timed
+    region, same mode): GB/s over the whole run by CUDA events and the SM
+    clocks sampled throughout (tens of samples, where the short timed region
+    gets a few)."""
+    import torch
+
+    import layout_aware_collectives_gb300 as tide
+
+    gptr = tide.PointerTable(job.grad_ptrs())
+    sptr = tide.PointerTable(job.shard_ptrs())
+    pptr = tide.PointerTable(job.param_ptrs())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):  # one step to size the run
+        e0.record(stream)
+        layout.reduce_scatter(gptr, sptr, wl.scale, stream)
+        layout.place(job.gathered, pptr, stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    steps = max(10, int(seconds * 1e3 / max(e0.elapsed_time(e1), 1e-3)))
+    clocks = ClockSampler(smi_dev)
+    clocks.start()
+    time.sleep(0.1)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            layout.reduce_scatter(gptr, sptr, wl.scale, stream)
+            layout.place(job.gathered, pptr, stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    clk = clocks.stop(t0, t1)
+    ms = e0.elapsed_time(e1)
+    return {"steps": steps, "seconds": round(ms * 1e-3, 3),
+            "GB/s": round(steps * (wl.rs_bytes() + wl.ag_bytes()) / (ms * 1e-3) / 1e9, 1), "clocks": clk}
+
+
 def mix_ratio(num_ranks: int) -> int:
     """Reads per write of the reduce-scatter (2N bytes read per 4 written),
     rounded to a ratio the HBM-mix probe has."""
@@ -476,6 +518,8 @@ def run_tide(args):
     }
 
     layout.check_device()  # raises if a bounded device wait ran out during the timed steps
+    if not args.no_sustained and rs_bytes + ag_bytes >= 2 * l2_bytes:  # no L2 flush between its steps
+        out["sustained"] = run_sustained(layout, job, wl, stream, smi_dev, world)
     layout.set_mode(tide.TIDE_MODE_UNCAPPED)
     if not args.no_next_ops:
         out["next_ops"] = run_next_ops(tide, layout, job, wl, stream)

@@ -1222,11 +1222,42 @@ def run_ipc(args):
     step_ms = reduce_max((time.perf_counter() - t0) * 1e3 / K, world)
     rs_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     ag_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    # each rank in turn, the others waiting at a barrier: its kernels alone on
+    # the GPU, reading its peers' memory through the IPC mappings
+    dims = [synth.dim0_inner(s) for s in wl.shapes]
+    valid_r = sum(lay.valid_rows(p, rank) * inner for p, (_, inner) in enumerate(dims))
+    turns = {}
+    for turn in range(world):
+        barrier(world)
+        if turn == rank:
+            with torch.cuda.stream(stream):
+                lay.reduce_scatter_rank(rank, gtab, stab, wl.scale, stream)
+                lay.place_ranks(btab, ptab, stream)
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                reps = 10
+                ev[0].record(stream)
+                for _ in range(reps):
+                    lay.reduce_scatter_rank(rank, gtab, stab, wl.scale, stream)
+                ev[1].record(stream)
+                for _ in range(reps):
+                    lay.place_ranks(btab, ptab, stream)
+                ev[2].record(stream)
+            torch.cuda.synchronize()
+            rs_t = ev[0].elapsed_time(ev[1]) / reps
+            pl_t = ev[1].elapsed_time(ev[2]) / reps
+            turns = {"rs_ms": round(rs_t, 4),
+                     "rs_GB/s": round((2 * world + 4) * valid_r / (rs_t * 1e-3) / 1e9, 1),
+                     "place_ms": round(pl_t, 4), "place_GB/s": round(4 * wl.psi / (pl_t * 1e-3) / 1e9, 1)}
+        barrier(world)
+    if world > 1:
+        every = [None] * world
+        dist.all_gather_object(every, turns)
+    else:
+        every = [turns]
     # bytes every rank moves per step: its reduce-scatter (N bf16 reads and one
     # fp32 write per valid element of its shards), its pack (6 bytes per
     # padded shard element) and the placement of every parameter (4 bytes per
     # element)
-    dims = [synth.dim0_inner(s) for s in wl.shapes]
     total_bytes = 0
     for r in range(world):
         valid = sum(lay.valid_rows(p, r) * inner for p, (_, inner) in enumerate(dims))
@@ -1243,6 +1274,10 @@ def run_ipc(args):
                          "step": "RS of this rank over every rank's gradients + pack + host barrier + "
                                  "placement from every rank's buffer + host barrier"},
               "rank0_kernels": {"rs_ms": round(rs_ms, 4), "place_ms": round(ag_ms, 4)},
+              "ranks_in_turn": every,
+              "ranks_in_turn_note": "each rank's single-rank reduce-scatter (over every rank's gradients, its "
+                                    "peers' through CUDA IPC) and per-rank placement timed alone on the GPU "
+                                    "while the other ranks wait",
               "note": "ranks share GPUs when there are fewer GPUs than ranks: a functional run of the "
                       "multi-process path, not a multi-GPU measurement"}, args)
     barrier(world)

@@ -94,16 +94,17 @@ __device__ __forceinline__ bool tile_ok(const Tile& t, int kind, const Extents& 
 // ---------------------------------------------------------------- reduce-scatter
 // One group of G ranks starting at rank k0: issue all G*V loads, then add
 // them in ascending rank order.  FULL means k0 + G <= N is known.
+// Vector u of a thread is vector v0 + u * stride of the run.
 template <int G, int V, bool FULL>
 __device__ __forceinline__ void rs_group(float (&acc)[V][8], const uint16_t* const* s_src, int k0,
-                                         int n, int v0, int nvec) {
+                                         int n, int v0, int nvec, int stride) {
   uint4 d[G][V];
 #pragma unroll
   for (int j = 0; j < G; ++j)
 #pragma unroll
     for (int u = 0; u < V; ++u)
-      if ((FULL || k0 + j < n) && v0 + u * (int)blockDim.x < nvec)
-        d[j][u] = ld_stream(s_src[k0 + j] + 8 * (v0 + u * (int)blockDim.x));
+      if ((FULL || k0 + j < n) && v0 + u * stride < nvec)
+        d[j][u] = ld_stream(s_src[k0 + j] + 8 * (v0 + u * stride));
 #pragma unroll
   for (int j = 0; j < G; ++j)
     if (FULL || k0 + j < n)
@@ -160,13 +161,13 @@ __global__ void __launch_bounds__(THREADS, TIDE_RS_MIN_BLOCKS) rs_kernel(RsArgs 
           for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
         if constexpr (NFIX > 0 && (THREADS <= 256 || NFIX <= G)) {
 #pragma unroll
-          for (int k0 = 0; k0 < NFIX; k0 += G) rs_group<G, V, true>(acc, sp, k0, N, v0, nvec);
+          for (int k0 = 0; k0 < NFIX; k0 += G) rs_group<G, V, true>(acc, sp, k0, N, v0, nvec, THREADS);
         } else if constexpr (NFIX > 0) {
           // fat CTAs: one group of loads in flight per thread, no spills
 #pragma unroll 1
-          for (int k0 = 0; k0 < NFIX; k0 += G) rs_group<G, V, true>(acc, sp, k0, N, v0, nvec);
+          for (int k0 = 0; k0 < NFIX; k0 += G) rs_group<G, V, true>(acc, sp, k0, N, v0, nvec, THREADS);
         } else {
-          for (int k0 = 0; k0 < N; k0 += G) rs_group<G, V, false>(acc, sp, k0, N, v0, nvec);
+          for (int k0 = 0; k0 < N; k0 += G) rs_group<G, V, false>(acc, sp, k0, N, v0, nvec, THREADS);
         }
 #pragma unroll
         for (int u = 0; u < V; ++u) {
@@ -187,6 +188,83 @@ __global__ void __launch_bounds__(THREADS, TIDE_RS_MIN_BLOCKS) rs_kernel(RsArgs 
       }
     } else {  // a run whose source is not 16-byte aligned: element by element
       for (int e = threadIdx.x; e < tile.len; e += THREADS) {
+        float acc = 0.f;
+        for (int k = 0; k < N; ++k) acc = __fadd_rn(acc, bf16_f32(ld_stream_u16(sp[k] + e)));
+        out[e] = __fmul_rn(acc, a.scale);
+      }
+    }
+  }
+}
+
+// CTA-capped form: every warp of the (few, fat) CTAs walks its own tiles —
+// tile t goes to warp t mod (warps in the grid) — with its N source pointers
+// in its own shared-memory slot, so no CTA-wide barrier ties the warps
+// together.  In the CTA-wide loop above, all of a fat CTA's warps issue
+// their loads, wait and add in step, and an SM holding one streams about
+// half of what its loads in flight allow; here, while some warps add, the
+// others' loads are in flight.  Same sums in the same order: each lane owns
+// whole 8-element vectors, strided by the warp width.  NFIX > 0 fixes N;
+// NFIX == 0 takes N at run time (N <= kRsWarpMaxRanks).
+template <int THREADS, int NFIX, int G, int V>
+__global__ void __launch_bounds__(THREADS, 1) rs_warp_kernel(RsArgs a) {
+  extern __shared__ const uint16_t* s_src[];  // [THREADS / 32][N] source pointers
+  const int N = NFIX > 0 ? NFIX : a.num_ranks;
+  const int lane = (int)threadIdx.x & 31, warp = (int)threadIdx.x >> 5;
+  const uint16_t** sp = s_src + warp * N;
+  constexpr int kWarps = THREADS / 32;
+  for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < a.num_tiles; t += (int64_t)gridDim.x * kWarps) {
+    const Tile tile = a.tiles[t];
+    if (!tile_ok(tile, a.kind, a.ext, a.err, lane == 0)) continue;  // uniform over the warp
+    float* __restrict__ out = a.stab[(int64_t)tile.r * a.num_params + tile.p] + tile.dst;
+
+    if (tile.flags & kTileZero) {  // padding rows of the shard
+      if (tile.flags & kTileVec) {
+        const int nv = tile.len >> 2;
+        for (int i = lane; i < nv; i += 32) st_stream(out + 4 * i, 0.f, 0.f, 0.f, 0.f);
+        for (int e = 4 * nv + lane; e < tile.len; e += 32) out[e] = 0.f;
+      } else {
+        for (int e = lane; e < tile.len; e += 32) out[e] = 0.f;
+      }
+      continue;
+    }
+
+    __syncwarp();  // every lane is done with the previous tile's pointers
+    for (int k = lane; k < N; k += 32) sp[k] = a.gtab[(int64_t)tile.p * N + k] + tile.src;
+    __syncwarp();
+
+    if (tile.flags & kTileVec) {
+      const int nvec = tile.len >> 3;
+      for (int v0 = lane; v0 < nvec; v0 += V * 32) {
+        float acc[V][8];
+#pragma unroll
+        for (int u = 0; u < V; ++u)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+        if constexpr (NFIX > 0) {
+#pragma unroll 1
+          for (int k0 = 0; k0 < NFIX; k0 += G) rs_group<G, V, true>(acc, sp, k0, N, v0, nvec, 32);
+        } else {
+          for (int k0 = 0; k0 < N; k0 += G) rs_group<G, V, false>(acc, sp, k0, N, v0, nvec, 32);
+        }
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          const int v = v0 + u * 32;
+          if (v < nvec) {
+            float* o = out + 8 * v;
+            st_stream(o, __fmul_rn(acc[u][0], a.scale), __fmul_rn(acc[u][1], a.scale),
+                      __fmul_rn(acc[u][2], a.scale), __fmul_rn(acc[u][3], a.scale));
+            st_stream(o + 4, __fmul_rn(acc[u][4], a.scale), __fmul_rn(acc[u][5], a.scale),
+                      __fmul_rn(acc[u][6], a.scale), __fmul_rn(acc[u][7], a.scale));
+          }
+        }
+      }
+      for (int e = 8 * nvec + lane; e < tile.len; e += 32) {
+        float acc = 0.f;
+        for (int k = 0; k < N; ++k) acc = __fadd_rn(acc, bf16_f32(ld_stream_u16(sp[k] + e)));
+        out[e] = __fmul_rn(acc, a.scale);
+      }
+    } else {  // a run whose source is not 16-byte aligned: element by element
+      for (int e = lane; e < tile.len; e += 32) {
         float acc = 0.f;
         for (int k = 0; k < N; ++k) acc = __fadd_rn(acc, bf16_f32(ld_stream_u16(sp[k] + e)));
         out[e] = __fmul_rn(acc, a.scale);
@@ -668,8 +746,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // One tile = a run of rank r's fp32 shard of parameter p, cast to bf16 into
 // its slot gathered[r*S + o_p + ...].  Per 8 elements: two 16-byte loads,
-// one 16-byte store.  WORKERS as in ag_kernel.
-template <int THREADS, int WORKERS>
+// one 16-byte store; each thread loads U such vectors before it stores any.
+// WORKERS as in ag_kernel.
+template <int THREADS, int WORKERS, int U>
 __global__ void __launch_bounds__(THREADS) pack_kernel(PackArgs a) {
   constexpr int WT = THREADS / WORKERS;
   static_assert(THREADS % WORKERS == 0 && WT % 32 == 0, "workers are whole warps");
@@ -683,15 +762,24 @@ __global__ void __launch_bounds__(THREADS) pack_kernel(PackArgs a) {
     int e0 = 0;
     if (tile.flags & kTileVec) {
       const int nvec = tile.len >> 3;
-      for (int v = lane; v < nvec; v += WT) {
-        const uint4 x = ld_stream(src + 8 * v);
-        const uint4 y = ld_stream(src + 8 * v + 4);
-        uint4 o;
-        o.x = pack2(__uint_as_float(x.x), __uint_as_float(x.y));
-        o.y = pack2(__uint_as_float(x.z), __uint_as_float(x.w));
-        o.z = pack2(__uint_as_float(y.x), __uint_as_float(y.y));
-        o.w = pack2(__uint_as_float(y.z), __uint_as_float(y.w));
-        st_stream(dst + 8 * v, o);
+      for (int v0 = lane; v0 < nvec; v0 += U * WT) {
+        uint4 x[U], y[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (v0 + u * WT < nvec) {
+            x[u] = ld_stream(src + 8 * (v0 + u * WT));
+            y[u] = ld_stream(src + 8 * (v0 + u * WT) + 4);
+          }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (v0 + u * WT < nvec) {
+            uint4 o;
+            o.x = pack2(__uint_as_float(x[u].x), __uint_as_float(x[u].y));
+            o.y = pack2(__uint_as_float(x[u].z), __uint_as_float(x[u].w));
+            o.z = pack2(__uint_as_float(y[u].x), __uint_as_float(y[u].y));
+            o.w = pack2(__uint_as_float(y[u].z), __uint_as_float(y[u].w));
+            st_stream(dst + 8 * (v0 + u * WT), o);
+          }
       }
       e0 = 8 * nvec;
     }
@@ -728,16 +816,50 @@ RsKernel rs_kernel_for(int32_t n, bool fat) {
   return fat ? rs_kernel_for<kFatThreads>(n) : rs_kernel_for<kRsThreads>(n);
 }
 
-// capped-mode CTAs: kFatThreads threads as groups of kAgThreads
-constexpr int kFatWorkers = kFatThreads / kAgThreads;
-static_assert(kFatThreads % kAgThreads == 0, "a fat CTA is whole placement groups");
+// Capped-mode kernels with per-warp tiles (N <= kRsWarpMaxRanks): the same
+// loads in flight per thread as the fat CTA-wide kernels.
+template <int T>
+RsKernel rs_warp_kernel_for(int32_t n) {
+  switch (n) {
+    case 1: return rs_warp_kernel<T, 1, 1, 8>;
+    case 2: return rs_warp_kernel<T, 2, 2, 4>;
+    case 3: return rs_warp_kernel<T, 3, 3, 2>;
+    case 4: return rs_warp_kernel<T, 4, 4, 2>;
+    case 5: return rs_warp_kernel<T, 5, 5, 1>;
+    case 6: return rs_warp_kernel<T, 6, 6, 1>;
+    case 7: return rs_warp_kernel<T, 7, 7, 1>;
+    case 8: return rs_warp_kernel<T, 8, 8, 1>;
+    case 16: return rs_warp_kernel<T, 16, 8, 1>;
+    case 32: return rs_warp_kernel<T, 32, 8, 1>;
+    case 64: return rs_warp_kernel<T, 64, 8, 1>;
+    default: return rs_warp_kernel<T, 0, 8, 1>;
+  }
+}
 
-AgKernel ag_kernel_for(bool fat, bool to_buf = false) {
-  if (to_buf)
-    return fat ? ag_kernel<kFatThreads, kFatWorkers, TIDE_AG_UNROLL, true>
-               : ag_kernel<kAgThreads, 1, TIDE_AG_UNROLL, true>;
-  return fat ? ag_kernel<kFatThreads, kFatWorkers, TIDE_AG_UNROLL, false>
-             : ag_kernel<kAgThreads, 1, TIDE_AG_UNROLL, false>;
+// Per-warp tiles for small capped grids.  Measured on GB300 (70B layer,
+// N = 8): 1.24-1.28x the CTA-wide loop at 8-64 CTAs, level at 96, 0.92x at
+// 152, where the kernel is bound by HBM rather than by each SM and the
+// CTA-wide loop's longer runs per rank stream better.
+bool rs_uses_warp_tiles(int32_t n, bool fat, int grid, int sms) {
+  return n <= kRsWarpMaxRanks && small_fat_grid(fat, grid, sms);
+}
+
+// capped-mode CTAs: kFatThreads threads as TIDE_FAT_WORKERS independent groups
+#ifndef TIDE_FAT_WORKERS
+#define TIDE_FAT_WORKERS (TIDE_FAT_THREADS / TIDE_AG_THREADS)
+#endif
+constexpr int kFatWorkers = TIDE_FAT_WORKERS;
+static_assert(kFatThreads % kFatWorkers == 0 && (kFatThreads / kFatWorkers) % 32 == 0,
+              "a fat CTA is whole groups of whole warps");
+
+// Small capped grids (small_fat_grid): every warp of a fat CTA is a group.
+constexpr int kFatWarpWorkers = kFatThreads / 32;
+
+template <bool TO_BUF>
+AgKernel ag_kernel_for(bool fat, bool warps) {
+  if (!fat) return ag_kernel<kAgThreads, 1, TIDE_AG_UNROLL, TO_BUF>;
+  return warps ? ag_kernel<kFatThreads, kFatWarpWorkers, TIDE_AG_FAT_UNROLL, TO_BUF>
+               : ag_kernel<kFatThreads, kFatWorkers, TIDE_AG_FAT_UNROLL, TO_BUF>;
 }
 
 }  // namespace
@@ -747,8 +869,13 @@ size_t rs_smem_bytes(int32_t num_ranks) { return 2 * sizeof(const uint16_t*) * (
 int rs_block(bool fat) { return fat ? kFatThreads : kRsThreads; }
 int ag_block(bool fat) { return fat ? kFatThreads : kAgThreads; }
 
-cudaError_t launch_rs(const RsArgs& a, int grid, bool fat, cudaStream_t stream) {
+cudaError_t launch_rs(const RsArgs& a, int grid, bool fat, int sms, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
+  if (rs_uses_warp_tiles(a.num_ranks, fat, grid, sms)) {
+    const size_t smem = sizeof(const uint16_t*) * (size_t)(kFatThreads / 32) * (size_t)a.num_ranks;
+    rs_warp_kernel_for<kFatThreads>(a.num_ranks)<<<grid, kFatThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+  }
   const RsKernel k = rs_kernel_for(a.num_ranks, fat);
   const size_t smem = rs_smem_bytes(a.num_ranks);
   if (smem > 48 * 1024) {  // 2*N staged pointers: above 3072 ranks they need the opt-in size
@@ -759,26 +886,31 @@ cudaError_t launch_rs(const RsArgs& a, int grid, bool fat, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
-cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, cudaStream_t stream) {
+// Placement and staging: in small capped grids one group per warp — measured
+// on GB300 (70B / MoE layers) 1.02x the two 512-thread groups at 8-32 CTAs,
+// 1.11-1.12x at 64, 0.96x at 152.
+cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, int sms, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
-  ag_kernel_for(fat)<<<grid, ag_block(fat), 0, stream>>>(a);
+  ag_kernel_for<false>(fat, small_fat_grid(fat, grid, sms))<<<grid, ag_block(fat), 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 int pk_block(bool fat) { return fat ? kFatThreads : kAgThreads; }
 
-cudaError_t launch_stage(const AgArgs& a, int grid, bool fat, cudaStream_t stream) {
+cudaError_t launch_stage(const AgArgs& a, int grid, bool fat, int sms, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
-  ag_kernel_for(fat, true)<<<grid, ag_block(fat), 0, stream>>>(a);
+  ag_kernel_for<true>(fat, small_fat_grid(fat, grid, sms))<<<grid, ag_block(fat), 0, stream>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, cudaStream_t stream) {
+cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, int sms, cudaStream_t stream) {
   if (grid <= 0 || a.num_tiles == 0) return cudaSuccess;
-  if (fat)
-    pack_kernel<kFatThreads, kFatWorkers><<<grid, kFatThreads, 0, stream>>>(a);
+  if (small_fat_grid(fat, grid, sms))
+    pack_kernel<kFatThreads, kFatWarpWorkers, TIDE_PACK_FAT_UNROLL><<<grid, kFatThreads, 0, stream>>>(a);
+  else if (fat)
+    pack_kernel<kFatThreads, kFatWorkers, TIDE_PACK_FAT_UNROLL><<<grid, kFatThreads, 0, stream>>>(a);
   else
-    pack_kernel<kAgThreads, 1><<<grid, kAgThreads, 0, stream>>>(a);
+    pack_kernel<kAgThreads, 1, 1><<<grid, kAgThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

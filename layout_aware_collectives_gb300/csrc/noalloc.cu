@@ -53,6 +53,7 @@ struct DeviceState {
   std::mutex mu;
   void* addr = nullptr;
   unsigned long long ctx = 0;  // id of the context `addr` and `held` belong to
+  int sms = 0;                 // the device's SM count
   Held held;
 };
 DeviceState g_dev[kMaxDevices];
@@ -103,6 +104,8 @@ tide_status_t device_state(std::unique_lock<std::mutex>* lock, DeviceState** out
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
     ctx = current_context_id();
     if (ctx == 0 || ctx != d.ctx) d.held = Held();  // another context: the contents are not ours
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
     d.addr = p;
     d.ctx = ctx;
   }
@@ -204,7 +207,7 @@ extern "C" TIDE_API tide_status_t tide_rs_bf16_to_fp32_noalloc(tide_layout_t l,
   a.num_ranks = N;
   a.num_params = P;
   a.scale = scale;
-  e = launch_rs(a, grid, l->mode == TIDE_MODE_CAPPED, stream);
+  e = launch_rs(a, grid, l->mode == TIDE_MODE_CAPPED, ds->sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter kernel launch");
   return TIDE_OK;
 }

@@ -439,7 +439,7 @@ tide_status_t run_rs(tide_layout_s* l, bool staged, int64_t t0, int64_t t1, cons
                                  (int64_t)l->num_ranks * slice_target));
   }
   cudaError_t e = rs_uses_bulk(l) ? launch_rs_bulk(a, grid_of(l, t1 - t0, 1), stream)
-                                  : launch_rs(a, grid_of(l, t1 - t0, 0), l->mode == TIDE_MODE_CAPPED,
+                                  : launch_rs(a, grid_of(l, t1 - t0, 0), l->mode == TIDE_MODE_CAPPED, l->num_sms,
                                               stream);
   if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter kernel launch");
   return mark_used(l, slot, stream);
@@ -489,8 +489,8 @@ cudaError_t launch_copy(tide_layout_s* l, AgArgs& a, bool to_buf, cudaStream_t s
   const bool capped = l->mode == TIDE_MODE_CAPPED;
   if (l->mode == TIDE_MODE_BULK)
     return launch_ag_bulk(a, grid_of(l, a.num_tiles, 0), to_buf, stream);
-  return to_buf ? launch_stage(a, grid_of(l, a.num_tiles, 0), capped, stream)
-                : launch_ag(a, grid_of(l, a.num_tiles, 0), capped, stream);
+  return to_buf ? launch_stage(a, grid_of(l, a.num_tiles, 0), capped, l->num_sms, stream)
+                : launch_ag(a, grid_of(l, a.num_tiles, 0), capped, l->num_sms, stream);
 }
 
 }  // namespace
@@ -664,7 +664,7 @@ tide_status_t tide_ag_place_ranks(tide_layout_t l, const uint16_t* const* gather
   // process's own memory): `cap` CTAs when capped, else one per tile
   const bool capped = l->mode == TIDE_MODE_CAPPED;
   const int grid = grid_for(a.num_tiles, capped ? TIDE_MODE_CAPPED : TIDE_MODE_UNCAPPED, l->cta_cap, l->num_sms, 0);
-  cudaError_t e = launch_ag(a, grid, capped, stream);
+  cudaError_t e = launch_ag(a, grid, capped, l->num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "placement kernel launch");
   return mark_used(l, slot, stream);
 }
@@ -714,7 +714,7 @@ tide_status_t tide_ag_pack_bf16(tide_layout_t l, int32_t rank, const float* cons
   a.num_params = P;
   a.err = l->d_err;
   a.ext = extents_of(l);
-  cudaError_t e = launch_pack(a, grid_of(l, t1 - t0, 0), l->mode == TIDE_MODE_CAPPED, stream);
+  cudaError_t e = launch_pack(a, grid_of(l, t1 - t0, 0), l->mode == TIDE_MODE_CAPPED, l->num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
   return mark_used(l, slot, stream);
 }

@@ -97,8 +97,17 @@ __host__ __device__ inline bool tile_in_range(const Tile& t, int kind, const Ext
 #ifndef TIDE_AG_TILE_ELEMS
 #define TIDE_AG_TILE_ELEMS 16384
 #endif
+#ifndef TIDE_AG_FAT_UNROLL  // 16-byte vectors a capped-mode placement thread loads before storing
+#define TIDE_AG_FAT_UNROLL 8
+#endif
+#ifndef TIDE_PACK_FAT_UNROLL  // 8-element vectors a capped-mode pack thread loads before storing
+#define TIDE_PACK_FAT_UNROLL 4
+#endif
 #ifndef TIDE_FAT_THREADS  // block of the CTA-capped mode: one fat CTA per occupied SM
 #define TIDE_FAT_THREADS 1024
+#endif
+#ifndef TIDE_WARP_TILES  // 1: small capped grids hand tiles to single warps, not to whole CTAs
+#define TIDE_WARP_TILES 1
 #endif
 #ifndef TIDE_RS_MIN_BLOCKS  // __launch_bounds__ min blocks per SM of the RS kernel
 #define TIDE_RS_MIN_BLOCKS 1
@@ -106,6 +115,9 @@ __host__ __device__ inline bool tile_in_range(const Tile& t, int kind, const Ext
 constexpr int kRsThreads = TIDE_RS_THREADS;
 constexpr int kAgThreads = TIDE_AG_THREADS;
 constexpr int kFatThreads = TIDE_FAT_THREADS;
+// Largest N the per-warp-tile capped reduce-scatter takes: its shared memory
+// holds N source pointers per warp (16 KiB at 1024 threads).
+constexpr int kRsWarpMaxRanks = 64;
 
 // Arguments of the reduce-scatter kernel.  gtab is param-major
 // (gtab[p * N + k] = rank k's gradient of p) so one tile's N pointers are
@@ -186,15 +198,22 @@ struct AgArgs {
 constexpr int kDevErrTimeout = 1;  // a bounded wait ran out
 constexpr int kDevErrRange = 2;    // debug builds: a tile failed tile_in_range and was skipped
 
+// A capped grid of at most half the device's SMs.  Each SM's own throughput
+// bounds such a grid, so its fat CTAs hand tiles to single warps, which run
+// out of step (one warp adds while the others' loads are in flight); larger
+// grids are bound by HBM, where whole-CTA tiles stream better.
+inline bool small_fat_grid(bool fat, int grid, int sms) { return TIDE_WARP_TILES && fat && 2 * (int64_t)grid <= sms; }
+
 // Kernel launchers (kernels.cu).  Return the launch's cudaError_t.  `fat`
 // selects the kFatThreads-wide CTA used by the CTA-capped mode: a capped CTA
 // takes its SM away from full-SM compute kernels anyway, so it brings as many
-// loads in flight as one SM holds.
-cudaError_t launch_rs(const RsArgs& a, int grid, bool fat, cudaStream_t stream);
-cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, cudaStream_t stream);
+// loads in flight as one SM holds.  `sms`: the device's SM count; a small
+// capped grid (small_fat_grid) hands its tiles to single warps.
+cudaError_t launch_rs(const RsArgs& a, int grid, bool fat, int sms, cudaStream_t stream);
+cudaError_t launch_ag(const AgArgs& a, int grid, bool fat, int sms, cudaStream_t stream);
 // The placement kernel run backwards (parameter storage -> rank-major
 // buffer): Slot-Reuse staging of gradients.  `buf` is written.
-cudaError_t launch_stage(const AgArgs& a, int grid, bool fat, cudaStream_t stream);
+cudaError_t launch_stage(const AgArgs& a, int grid, bool fat, int sms, cudaStream_t stream);
 // Bulk-copy (TMA engine) placement / staging: one issuing lane per CTA,
 // shared-memory ring of TIDE_BULK_STAGES x TIDE_BULK_CHUNK bytes.
 cudaError_t launch_ag_bulk(const AgArgs& a, int grid, bool to_buf, cudaStream_t stream);
@@ -203,7 +222,7 @@ cudaError_t launch_ag_bulk(const AgArgs& a, int grid, bool to_buf, cudaStream_t 
 constexpr int kRsBulkMaxRanks = 1024;  // bulk RS runs for N <= kRsBulkMaxRanks / 2
 constexpr int kRsBulkThreads = 288;
 cudaError_t launch_rs_bulk(const RsArgs& a, int grid, cudaStream_t stream);
-cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, cudaStream_t stream);
+cudaError_t launch_pack(const PackArgs& a, int grid, bool fat, int sms, cudaStream_t stream);
 int rs_block(bool fat);
 int ag_block(bool fat);
 int pk_block(bool fat);

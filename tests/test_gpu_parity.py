@@ -22,7 +22,7 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU-only ho
 import layout_aware_collectives_gb300 as tide  # noqa: E402
 
 MODES = [("uncapped", tide.TIDE_MODE_UNCAPPED, 0)] + [
-    (f"capped{c}", tide.TIDE_MODE_CAPPED, c) for c in (1, 2, 7, 8, 32)] + [
+    (f"capped{c}", tide.TIDE_MODE_CAPPED, c) for c in (1, 2, 7, 8, 32, 120)] + [
     ("bulk_cap3", tide.TIDE_MODE_BULK, 3), ("bulk", tide.TIDE_MODE_BULK, 0)]
 
 
@@ -339,13 +339,15 @@ def test_full_size_sampled_parity(name):
         gpu_checks.torch_check_rs(job)
         del job.slots
 
-        lay.set_mode(tide.TIDE_MODE_CAPPED, 64)
-        clear_outputs()
-        run(job)
-        assert gpu_checks.sampled_check_rs(job, seed=2) > 0
-        assert gpu_checks.sampled_check_ag(job, seed=2) > 0
-        gpu_checks.torch_check_rs(job)
-        gpu_checks.torch_check_ag(job)
+        # capped grids of at most half the SMs hand tiles to single warps; larger ones to whole CTAs
+        for cap in (64, 152):
+            lay.set_mode(tide.TIDE_MODE_CAPPED, cap)
+            clear_outputs()
+            run(job)
+            assert gpu_checks.sampled_check_rs(job, seed=cap) > 0
+            assert gpu_checks.sampled_check_ag(job, seed=cap) > 0
+            gpu_checks.torch_check_rs(job)
+            gpu_checks.torch_check_ag(job)
         # TMA bulk-staged reduce-scatter and bulk-copy placement, capped and over every SM
         for cap in (16, 0):
             lay.set_mode(tide.TIDE_MODE_BULK, cap)

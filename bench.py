@@ -612,6 +612,9 @@ def run_hbm_mix(ratios, smi_dev, out_bytes=1 << 30, reps=10):
     lib.hbm_read.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
     lib.hbm_write.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p]
     lib.hbm_mix.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    lib.hbm_sm_stream.restype = ctypes.c_int
+    lib.hbm_sm_stream.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_void_p, ctypes.c_void_p]
     rmax = max([1] + list(ratios))
     src = torch.empty(max(rmax, 4) * out_bytes, dtype=torch.uint8, device="cuda")
     dst = torch.empty(out_bytes, dtype=torch.uint8, device="cuda")
@@ -648,6 +651,15 @@ def run_hbm_mix(ratios, smi_dev, out_bytes=1 << 30, reps=10):
     for r in sorted({1} | set(ratios)):
         res[f"read{r}_write1"] = rate(lambda r=r: lib.hbm_mix(src.data_ptr(), dst.data_ptr(), out_bytes, r, sh),
                                       (r + 1) * out_bytes)
+    # what one SM moves: 8 persistent 1024-thread CTAs (the CTA-capped kernels' shape), per CTA
+    half = out_bytes // 2
+    per_cta = {}
+    for name, mode, nbytes in (("read", 0, half), ("write", 1, half), ("copy_read_plus_write", 2, 2 * half)):
+        gbs = rate(lambda mode=mode: lib.hbm_sm_stream(src.data_ptr(), dst.data_ptr(), half, mode, 8,
+                                                       sink.data_ptr(), sh), nbytes)
+        per_cta[name] = round(gbs / 8, 1)
+    res["per_sm_8_ctas"] = {"kernel": "bench_hbm.cu hbm_sm_stream: 8 CTAs x 1024 threads, 8 accesses in "
+                                      "flight per thread; GB/s per CTA (each CTA holds one SM)", **per_cta}
     t1 = time.time()
     rd, wr = res["read_only"], res["write_only"]
     # the rate a stream with read fraction f would reach if reads ran at the

@@ -9,6 +9,8 @@
 // stream above the 1:1 figure.  These streams measure what a read-only, a
 // write-only and an R:1 read:write stream of the same shape reach on this
 // GPU, so the reduce-scatter can be compared with a ceiling of its own mix.
+// The few-CTA streams measure what one SM moves, the bound of the CTA-capped
+// kernels.
 //
 // Used only by bench.py; not part of the library.
 #include <cuda_runtime.h>
@@ -101,6 +103,46 @@ __global__ void __launch_bounds__(kThreads) mix_kernel(const uint4* src, uint4* 
   }
 }
 
+// Few-CTA streams, the shape of the CTA-capped kernels: `grid` CTAs of 1024
+// threads loop over the buffer, every thread with 8 16-byte accesses in
+// flight, so each CTA holds an SM and the rate per CTA is what one SM
+// moves.  MODE 0 reads (XOR kept as in read_kernel), 1 writes, 2 copies.
+constexpr int kSmThreads = 1024;
+constexpr int kSmVec = 8;
+template <int MODE>
+__global__ void __launch_bounds__(kSmThreads, 1) sm_stream_kernel(const uint4* src, uint4* dst, int64_t nvec,
+                                                                  uint4* sink) {
+  constexpr int64_t kChunk = (int64_t)kSmThreads * kSmVec;
+  uint4 acc = make_uint4(0, 0, 0, 0);
+  for (int64_t base = (int64_t)blockIdx.x * kChunk; base < nvec; base += (int64_t)gridDim.x * kChunk) {
+    if constexpr (MODE == 1) {
+#pragma unroll
+      for (int u = 0; u < kSmVec; ++u) {
+        const int64_t i = base + threadIdx.x + (int64_t)u * kSmThreads;
+        if (i < nvec) st_stream(dst + i, make_uint4((uint32_t)i, 1u, 2u, 3u));
+      }
+    } else {
+      uint4 d[kSmVec];
+#pragma unroll
+      for (int u = 0; u < kSmVec; ++u) {
+        const int64_t i = base + threadIdx.x + (int64_t)u * kSmThreads;
+        d[u] = i < nvec ? ld_stream(src + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kSmVec; ++u) {
+        const int64_t i = base + threadIdx.x + (int64_t)u * kSmThreads;
+        if constexpr (MODE == 2) {
+          if (i < nvec) st_stream(dst + i, d[u]);
+        } else {
+          xor_into(acc, d[u]);
+        }
+      }
+    }
+  }
+  if (MODE == 0 && acc.x == 0x9E3779B9u && acc.y == 0x7F4A7C15u && acc.z == 0xF39CC060u && acc.w == 0x5CEDC834u)
+    sink[0] = acc;
+}
+
 int grid_of(int64_t nvec) { return (int)((nvec + kTileVecs - 1) / kTileVecs); }
 
 }  // namespace
@@ -138,6 +180,23 @@ HBM_API int hbm_mix(const void* src, void* dst, int64_t out_bytes, int ratio, cu
     case 4: mix_kernel<4, 2><<<g, kThreads, 0, stream>>>(s, d, nvec); break;
     case 8: mix_kernel<8, 1><<<g, kThreads, 0, stream>>>(s, d, nvec); break;
     case 16: mix_kernel<16, 1><<<g, kThreads, 0, stream>>>(s, d, nvec); break;
+    default: return (int)cudaErrorInvalidValue;
+  }
+  return (int)cudaGetLastError();
+}
+
+// `grid` persistent 1024-thread CTAs streaming `bytes`: mode 0 reads src,
+// 1 writes dst, 2 copies src to dst (bytes read and bytes written each).
+HBM_API int hbm_sm_stream(const void* src, void* dst, int64_t bytes, int mode, int grid, void* sink16,
+                          cudaStream_t stream) {
+  const int64_t nvec = bytes / 16;
+  if (nvec <= 0 || grid <= 0) return 0;
+  const uint4* s = (const uint4*)src;
+  uint4* d = (uint4*)dst;
+  switch (mode) {
+    case 0: sm_stream_kernel<0><<<grid, kSmThreads, 0, stream>>>(s, d, nvec, (uint4*)sink16); break;
+    case 1: sm_stream_kernel<1><<<grid, kSmThreads, 0, stream>>>(s, d, nvec, (uint4*)sink16); break;
+    case 2: sm_stream_kernel<2><<<grid, kSmThreads, 0, stream>>>(s, d, nvec, (uint4*)sink16); break;
     default: return (int)cudaErrorInvalidValue;
   }
   return (int)cudaGetLastError();

@@ -74,11 +74,11 @@
  *    stream; the compute's stream must be raised, which only the caller can
  *    do.  Measured on GB300
  *    beside a loop of bf16 8192^3 GEMMs over 0.3 s windows (power-capped
- *    clock; 70B- and MoE-shaped layers): equal priority +279% to +593%
+ *    clock; 70B- and MoE-shaped layers): equal priority +279% to +601%
  *    GEMM time, depending on how the launches are submitted; low priority
- *    +7.2% to +9.6% with the reduce-scatter moving 0.28-0.33 TB/s, about
- *    what 8 capped CTAs cost (+7.4% to +9.2%, 0.37-0.39 TB/s); capped
- *    16 / 32 / 64 CTAs +13-15% / +23-25% / +50-53%.
+ *    +7.2% to +9.6% with the reduce-scatter moving 0.28-0.35 TB/s, about
+ *    what 8 capped CTAs cost (+6.8% to +8.6%, 0.41-0.44 TB/s); capped
+ *    16 / 32 / 64 CTAs +12-13% / +22-23% / +49-50%.
  *  - A layout may be used from several host threads (calls are serialised
  *    internally).  Calls on different streams that write the same output
  *    buffers race, as any two kernels would.
@@ -127,8 +127,12 @@ typedef enum {
    * list: the short-lived-CTA budget of "TIDE的设计思路", trading bandwidth
    * for SM time left to concurrent compute.  Each CTA is 1024 threads wide
    * (an SM hosting one is lost to full-SM compute kernels anyway, so it
-   * keeps a whole SM's loads in flight); in the placement, staging and pack
-   * it is two 512-thread groups, each walking its own tiles. */
+   * keeps a whole SM's loads in flight).  In a grid of at most half the
+   * SMs every warp walks its own tiles (the reduce-scatter for N <= 64,
+   * and the placement, staging and pack), so one SM moves about 110 GB/s
+   * of reduce-scatter traffic at N = 8 on GB300; larger grids hand each
+   * tile to a whole CTA (placement, staging, pack: two 512-thread groups).
+   * Results are the same in every form. */
   TIDE_MODE_CAPPED = 1,
   /* Placement and Slot-Reuse staging through the copy engines
    * (cudaMemcpy2DAsync, no SM use), the copy-engine path of "TIDE的设计思路".

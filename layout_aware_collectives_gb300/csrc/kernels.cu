@@ -279,8 +279,8 @@ __global__ void __launch_bounds__(THREADS, 1) rs_warp_kernel(RsArgs a) {
 // vectors per thread are loaded before any is stored.  TO_BUF runs the same
 // copy backwards (Slot-Reuse staging of a gradient into the rank-major slot).
 // A CTA is WORKERS independent groups of THREADS / WORKERS threads, each
-// walking its own tiles (a capped-mode CTA is two tile-sized groups, so one
-// pass of each group covers a whole tile).
+// walking its own tiles: one group per CTA over every SM; in capped mode one
+// per warp in small grids (small_fat_grid), else two 512-thread groups.
 template <int THREADS, int WORKERS, int U, bool TO_BUF>
 __global__ void __launch_bounds__(THREADS) ag_kernel(AgArgs a) {
   constexpr int WT = THREADS / WORKERS;
@@ -523,9 +523,12 @@ __global__ void __launch_bounds__(32) ag_bulk_kernel(AgArgs a) {
 // "full" mbarrier.  Warps 1..8 consume: wait for "full", sum the N slices in
 // ascending rank order from shared memory (__fadd_rn, the same sequence as
 // the load/store kernel), write the fp32 results with streaming stores, and
-// release the stage on its "empty" mbarrier.  With ~192 KiB of slices in
-// flight per SM a CTA moves more bytes per SM than registers allow, which is
-// what a CTA-capped run is limited by.  Zero tiles, unaligned runs and the
+// release the stage on its "empty" mbarrier.  The bulk-copy engine keeps
+// ~192 KiB of slices in flight per SM with a seventh of the load/store
+// kernel's warps resident (measured on GB300: 0.96-0.97 of its bandwidth
+// over every SM, and per SM in a capped run 80 GB/s against the per-warp
+// tile kernel's 110: there the SM's path out to L2 is the limit, not bytes
+// in flight).  Zero tiles, unaligned runs and the
 // < 8 element tails of vector runs are done by the consumers with plain
 // loads.  Every wait is bounded as in the bulk-copy placement.
 namespace bulk {

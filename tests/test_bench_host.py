@@ -11,7 +11,7 @@ import bench
 
 def test_hbm_probe_library_exports_its_entry_points():
     lib = ctypes.CDLL(bench.HBM_LIB)
-    for name in ("hbm_read", "hbm_write", "hbm_mix"):
+    for name in ("hbm_read", "hbm_write", "hbm_mix", "hbm_sm_stream"):
         assert hasattr(lib, name), name
 
 

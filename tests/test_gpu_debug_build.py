@@ -33,8 +33,9 @@ import oracle
 import synth
 from synth.device import DeviceJob
 
-MODES = [(tide.TIDE_MODE_UNCAPPED, 0), (tide.TIDE_MODE_CAPPED, 3), (tide.TIDE_MODE_BULK, 0),
-         (tide.TIDE_MODE_BULK, 3), (tide.TIDE_MODE_COPY_ENGINE, 0)]
+# capped 3: per-warp tiles; capped 120: whole-CTA tiles wherever the list has more than 76 tiles
+MODES = [(tide.TIDE_MODE_UNCAPPED, 0), (tide.TIDE_MODE_CAPPED, 3), (tide.TIDE_MODE_CAPPED, 120),
+         (tide.TIDE_MODE_BULK, 0), (tide.TIDE_MODE_BULK, 3), (tide.TIDE_MODE_COPY_ENGINE, 0)]
 
 
 def cases():

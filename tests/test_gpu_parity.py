@@ -239,6 +239,32 @@ def _staged(job, modes, scale=None):
         assert job.guards_intact()
 
 
+def test_capped_forms_on_both_sides_of_half_the_sms(tiny_job):
+    """Capped grids of at most half the SMs hand tiles to single warps and
+    larger ones to whole CTAs: caps just below, at and above that boundary,
+    and one CTA per SM, give the oracle's results in every capped operation
+    (reduce-scatter, placement, pack, staging, staged reduce-scatter).  The
+    tiny block's lists hold more tiles than any cap here, so each cap is the
+    launched grid."""
+    job = tiny_job
+    lay = job.layout
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    half = sms // 2
+    for op in (tide.TIDE_OP_RS, tide.TIDE_OP_AG, tide.TIDE_OP_PACK, tide.TIDE_OP_STAGE, tide.TIDE_OP_STAGED_RS):
+        assert len(lay.tiles(op)) > sms, op
+    caps = [(f"capped{c}", tide.TIDE_MODE_CAPPED, c) for c in (half - 1, half, half + 1, sms)]
+    for mode in caps:
+        lay.set_mode(*mode[1:])
+        assert lay.launch_shape(tide.TIDE_OP_RS) == (mode[2], 1024)
+        job.reset_outputs()
+        run(job)
+        gpu_checks.full_check_rs(job)
+        gpu_checks.full_check_ag(job)
+        assert job.guards_intact()
+    _rank_rs_and_pack(job, caps[1:3])
+    _staged(job, caps[1:3])
+
+
 STAGE_MODES = MODES[:3] + [("bulk", tide.TIDE_MODE_BULK, 0),
                            ("copy_engine", tide.TIDE_MODE_COPY_ENGINE, 0)]
 

@@ -814,6 +814,7 @@ def run_stock(job, wl, stream, tide_rs_ms, tide_ag_ms, reps=10):
 
     st = StockFSDP2(job)
     torch.cuda.synchronize()  # set-up work ran on the default stream
+    flat_bytes = sum(t.numel() * t.element_size() for t in st.flat)
     N, psi, padded = wl.num_ranks, wl.psi, sum(job.shard_numel)
     flat = N * padded  # elements of one rank's flat buffer (every destination block)
     parts = {"rs_copy_in": (st.copy_in, N * (2 * psi + 4 * flat)),
@@ -840,6 +841,24 @@ def run_stock(job, wl, stream, tide_rs_ms, tide_ag_ms, reps=10):
     res["tide_speedup_vs_stock"] = round(total / (tide_rs_ms + tide_ag_ms), 2)
     res["note"] = ("stock = chunk_cat copy-in (bf16->fp32) + torch rank-order fp32 sum of flat "
                    "buffers + split_with_sizes_copy copy-out; TIDE = fused RS + placement")
+    # Device memory beyond what both paths hold (gradients, shards, the
+    # rank-major all-gather buffer, parameters), per rank.  Stock: the fp32
+    # flat reduce-scatter input.  TIDE: the reduce-scatter reads the gradients in
+    # place and Slot-Reuse stages them into the vacated all-gather slot, so
+    # neither needs a buffer; the library's own device state is its tile
+    # lists and cached pointer tables.  (Stock: the flat tensors' sizes over
+    # the N simulated ranks, divided by N.)
+    import layout_aware_collectives_gb300 as tide
+
+    lay = job.layout
+    tile_bytes = 32 * sum(len(lay.tiles(op)) for op in (tide.TIDE_OP_RS, tide.TIDE_OP_AG, tide.TIDE_OP_PACK,
+                                                          tide.TIDE_OP_STAGED_RS))
+    res["memory_per_rank"] = {
+        "stock_rs_input_bytes": flat_bytes // N,
+        "tide_rs_extra_bytes": 0,
+        "slot_reuse_extra_bytes": 0,
+        "tide_library_device_bytes": {"tile_lists": tile_bytes,
+                                      "per_cached_pointer_table": 16 * N * job.P, "max_cached_tables": 8}}
     del st
     torch.cuda.empty_cache()
     return res

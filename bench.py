@@ -853,6 +853,17 @@ def run_stock(job, wl, stream, tide_rs_ms, tide_ag_ms, reps=10):
     lay = job.layout
     tile_bytes = 32 * sum(len(lay.tiles(op)) for op in (tide.TIDE_OP_RS, tide.TIDE_OP_AG, tide.TIDE_OP_PACK,
                                                           tide.TIDE_OP_STAGED_RS))
+    # SM time (kernel time x SMs occupied; every launch here spans the GPU),
+    # the analog of the pages' reduce-scatter SM-time comparison
+    # ("FSDP通信终局：TIDE零拷贝集合通信优化" §性能表现)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    stock_rs = res["rs_copy_in"]["ms"] + res["flat_reduce"]["ms"]
+    res["sm_ms"] = {"stock_rs_copy_in_plus_flat_reduce": round(stock_rs * sms, 1),
+                    "stock_flat_reduce": round(res["flat_reduce"]["ms"] * sms, 1),
+                    "tide_rs": round(tide_rs_ms * sms, 1),
+                    "stock_rs_over_tide_rs": round(stock_rs / tide_rs_ms, 2),
+                    "note": "kernel ms x SMs occupied (all of them for these launches); the CTA-capped "
+                            "reduce-scatter's SM.ms is in the interference table"}
     res["memory_per_rank"] = {
         "stock_rs_input_bytes": flat_bytes // N,
         "tide_rs_extra_bytes": 0,

@@ -78,7 +78,7 @@
  *    GEMM time, depending on how the launches are submitted; low priority
  *    +7.2% to +9.6% with the reduce-scatter moving 0.28-0.35 TB/s, about
  *    what 8 capped CTAs cost (+6.8% to +8.6%, 0.41-0.44 TB/s); capped
- *    16 / 32 / 64 CTAs +12-14% / +22-24% / +49-50%.
+ *    16 / 32 / 64 CTAs +12-14% / +22-26% / +49-51%.
  *  - A layout may be used from several host threads (calls are serialised
  *    internally).  Calls on different streams that write the same output
  *    buffers race, as any two kernels would.
